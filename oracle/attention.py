@@ -1,0 +1,134 @@
+"""fp64 oracle: scaled dot-product self-attention over a packed THD batch.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+What is computed (written from the pages' definitions, not from any kernel):
+
+* Layout ("How to pad sequences ... context parallelism", repro script): Q, K, V
+  are ``[t, h, d]`` tensors; all sequences of the batch are concatenated along
+  the token axis.
+* Boundaries ("Add per-sequence causal policy ...", ``pad_between_seqs``
+  review comment): sequence ``b`` has ``cu_seqlens[b+1] - cu_seqlens[b]``
+  valid tokens.  With ``cu_seqlens_padded`` its tokens start at row
+  ``cu_seqlens_padded[b]`` of the packed buffer; the rows up to the next start
+  are padding.  Without it, sequence ``b`` starts at ``cu_seqlens[b]``.
+  Only the first ``batch_size + 1`` entries are read (the slice rule of
+  "[PyTorch] Build the attention padding mask ...", Changes).
+* Policy ("Add per-sequence causal policy ...", Changes): one boolean per
+  sequence.  True selects ``padding_causal`` (key ``j`` visible to query ``i``
+  iff ``j <= i``, positions counted from the sequence's first token); False
+  selects ``padding`` (every valid key visible).
+* Output: for each valid query row ``softmax(scale * q k^T) v`` over the
+  visible keys; every row that belongs to no sequence is 0 (the example's
+  "0s on pad positions").  The log-sum-exp ``lse = log(sum_j exp(scale*q.k_j))``
+  (natural log, scale included) is returned per (head, row), ``-inf`` on pad
+  rows and on rows with no visible key.
+* Grouped-query heads: query head ``h`` reads key/value head
+  ``h // (Hq // Hkv)``.
+
+Arithmetic is fp64 throughout; the inputs are the exact bf16/fp16 values,
+upcast.  Query rows are processed in blocks of ``row_block`` with a plain
+matrix product (numpy ``@``): no online softmax, no reordering of the
+definition beyond the standard max-shift used to evaluate ``exp`` safely.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _as64(x):
+    if hasattr(x, "detach"):  # torch tensor -> numpy without importing torch here
+        x = x.detach().cpu().float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def sequence_spans(cu_seqlens, cu_seqlens_padded, batch_size):
+    """(start_row, length) of every sequence; reads only entries 0..batch_size."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)[: batch_size + 1]
+    lengths = cu[1:] - cu[:-1]
+    if cu_seqlens_padded is None:
+        starts = cu[:-1].copy()
+    else:
+        starts = np.asarray(cu_seqlens_padded, dtype=np.int64)[:batch_size].copy()
+    return starts, lengths
+
+
+def _one_sequence(q, k, v, causal, scale, row_ids=None):
+    """softmax(scale q k^T [+ causal]) v for one (sequence, head).
+
+    q: [L, d], k/v: [L, d] fp64.  ``row_ids`` selects query rows (default all).
+    Returns (out [n, d], lse [n]).
+    """
+    L = k.shape[0]
+    rows = np.arange(q.shape[0]) if row_ids is None else np.asarray(row_ids)
+    z = scale * (q[rows] @ k.T)                     # [n, L] logits
+    if causal:
+        visible = np.arange(L)[None, :] <= rows[:, None]
+        z = np.where(visible, z, -np.inf)
+    zmax = z.max(axis=1, keepdims=True)
+    e = np.exp(z - zmax)
+    s = e.sum(axis=1, keepdims=True)
+    lse = (zmax + np.log(s))[:, 0]
+    out = (e / s) @ v
+    return out, lse
+
+
+def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                      cu_seqlens_kv_padded, seq_is_causal, batch_size, softmax_scale,
+                      row_block=1024):
+    """Whole-batch oracle.  Returns (out [T, Hq, d] fp64, lse [Hq, T] fp64).
+
+    ``seq_is_causal`` may be None (every sequence full-context).  Self-attention
+    is assumed: ``cu_seqlens_q`` and ``cu_seqlens_kv`` describe the same
+    sequences (the lengths must agree).
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    group = Hq // Hkv
+    qs, ql = sequence_spans(cu_seqlens_q, cu_seqlens_q_padded, batch_size)
+    ks, kl = sequence_spans(cu_seqlens_kv, cu_seqlens_kv_padded, batch_size)
+    if not np.array_equal(ql, kl):
+        raise ValueError("oracle covers self-attention: q and kv lengths must agree")
+    flags = (np.zeros(batch_size, dtype=bool) if seq_is_causal is None
+             else np.asarray(seq_is_causal)[:batch_size].astype(bool))
+    out = np.zeros((T, Hq, d), dtype=np.float64)
+    lse = np.full((Hq, T), -np.inf, dtype=np.float64)
+    for b in range(batch_size):
+        L = int(ql[b])
+        if L <= 0:
+            continue
+        s0, k0 = int(qs[b]), int(ks[b])
+        for h in range(Hq):
+            g = h // group
+            kk = k[k0:k0 + L, g, :]
+            vv = v[k0:k0 + L, g, :]
+            qq = q[s0:s0 + L, h, :]
+            for r0 in range(0, L, row_block):
+                rows = np.arange(r0, min(L, r0 + row_block))
+                o, m = _one_sequence(qq, kk, vv, bool(flags[b]), softmax_scale, rows)
+                out[s0 + rows, h, :] = o
+                lse[h, s0 + rows] = m
+    return out, lse
+
+
+def thd_attention_rows(q, k, v, start_q, start_kv, length, causal, head, group,
+                       softmax_scale, row_ids):
+    """Oracle values for selected query rows of one (sequence, head).
+
+    Used to check full-size batches on sampled rows.  ``row_ids`` are positions
+    inside the sequence (0-based).  ``q``/``k``/``v`` are the full packed
+    tensors (torch or numpy).  Returns (out [n, d], lse [n]) in fp64.
+    """
+    g = head // group
+    rows = np.asarray(row_ids, dtype=np.int64)
+    qq = _as64(q[start_q + rows, head, :])
+    kk = _as64(k[start_kv:start_kv + length, g, :])
+    vv = _as64(v[start_kv:start_kv + length, g, :])
+    z = softmax_scale * (qq @ kk.T)
+    if causal:
+        z = np.where(np.arange(length)[None, :] <= rows[:, None], z, -np.inf)
+    zmax = z.max(axis=1, keepdims=True)
+    e = np.exp(z - zmax)
+    s = e.sum(axis=1, keepdims=True)
+    return (e / s) @ vv, (zmax + np.log(s))[:, 0]

@@ -1,0 +1,101 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that some pin catches each.
+
+Each mutant replaces one helper of ``oracle.attention`` for the duration of a test;
+the pins of ``test_oracle_pins`` are then run and at least one must fail.
+"""
+import numpy as np
+import pytest
+
+import oracle.attention as oa
+import test_oracle_pins as pins
+
+PINS = [
+    pins.test_page1_printed_values,
+    pins.test_page1_closed_form_full,
+    pins.test_page1_closed_form_causal,
+    pins.test_page1_pad_row_is_zero_and_ignored,
+    pins.test_mixed_policy_equals_per_sequence_scalar_policy,
+    pins.test_two_call_pad_between_seqs_sum,
+    pins.test_brute_force_scalar_loops,
+    pins.test_gqa_against_torch_sdpa_fp64,
+    pins.test_causal_first_row_is_first_value_and_rows_are_convex,
+]
+
+
+def _softmax_rows(z, v):
+    zmax = z.max(axis=1, keepdims=True)
+    e = np.exp(z - zmax)
+    s = e.sum(axis=1, keepdims=True)
+    return (e / s) @ v, (zmax + np.log(s))[:, 0]
+
+
+def strict_causal(q, k, v, causal, scale, row_ids=None):
+    rows = np.arange(q.shape[0]) if row_ids is None else np.asarray(row_ids)
+    z = scale * (q[rows] @ k.T)
+    if causal:  # mistake: the diagonal is hidden (j < i), row 0 sees nothing
+        z = np.where(np.arange(k.shape[0])[None, :] < rows[:, None], z, -1e300)
+    return _softmax_rows(z, v)
+
+
+def no_scale(q, k, v, causal, scale, row_ids=None):
+    rows = np.arange(q.shape[0]) if row_ids is None else np.asarray(row_ids)
+    z = q[rows] @ k.T   # mistake: scale dropped
+    if causal:
+        z = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], z, -np.inf)
+    return _softmax_rows(z, v)
+
+
+def bottom_right(q, k, v, causal, scale, row_ids=None):
+    rows = np.arange(q.shape[0]) if row_ids is None else np.asarray(row_ids)
+    z = scale * (q[rows] @ k.T)
+    if causal:  # mistake: causal mask anchored at the other corner of a rectangular block
+        off = k.shape[0] - q.shape[0] + 1
+        z = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None] + off, z, -np.inf)
+    return _softmax_rows(z, v)
+
+
+def lse_without_max(q, k, v, causal, scale, row_ids=None):
+    out, lse = pins_free_reference(q, k, v, causal, scale, row_ids)
+    z = scale * (q @ k.T)
+    return out, lse - z.max()  # mistake: the max shift is dropped from the LSE
+
+
+def pins_free_reference(q, k, v, causal, scale, row_ids=None):
+    rows = np.arange(q.shape[0]) if row_ids is None else np.asarray(row_ids)
+    z = scale * (q[rows] @ k.T)
+    if causal:
+        z = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], z, -np.inf)
+    return _softmax_rows(z, v)
+
+
+def transposed_values(q, k, v, causal, scale, row_ids=None):
+    rows = np.arange(q.shape[0]) if row_ids is None else np.asarray(row_ids)
+    z = scale * (q[rows] @ k.T)
+    if causal:
+        z = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], z, -np.inf)
+    o, l = _softmax_rows(z, k)   # mistake: weights applied to K instead of V
+    return o, l
+
+
+def starts_from_cu(cu_seqlens, cu_seqlens_padded, batch_size):
+    cu = np.asarray(cu_seqlens, dtype=np.int64)[: batch_size + 1]
+    return cu[:-1].copy(), cu[1:] - cu[:-1]   # mistake: padded offsets ignored
+
+
+@pytest.mark.parametrize("target,mutant", [
+    ("_one_sequence", strict_causal),
+    ("_one_sequence", no_scale),
+    ("_one_sequence", bottom_right),
+    ("_one_sequence", lse_without_max),
+    ("_one_sequence", transposed_values),
+    ("sequence_spans", starts_from_cu),
+])
+def test_pins_catch_mutant(monkeypatch, target, mutant):
+    monkeypatch.setattr(oa, target, mutant)
+    failed = 0
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
