@@ -1,0 +1,430 @@
+"""Benchmark: packed THD attention forward (+ padding mask) on GB300.
+
+One step = the whole hot path over one synthetic packed batch: thd_attn_fwd on the
+long-context workload (8 sequences, 131072 tokens, 16 heads, d=128, bf16, 6 causal /
+2 full-context, metadata buffers sized for 64 sequences) followed by thd_padding_mask
+for the same cu_seqlens.  `value` is effective attention TFLOP/s over all ranks
+(4*d*Hq per unmasked query-key pair), inputs resident in HBM.  The padding mask is also
+timed alone on the 4096 x 8192 mask workload (GB/s against HBM peak).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica of the workload (weak scaling, no
+collective on the data path; the barrier and max-over-ranks timing use the process
+group).  `--impl reference` times the fp64 CPU oracle on host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+_NCORES = len(os.sched_getaffinity(0))
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_NCORES))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "THD attn fwd effective TFLOP/s and % of GB300 dense BF16 peak; mask GB/s"
+WORKLOAD = "long_context"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["variable_length_packed_gb300/csrc/" + f for f in
+                  ("ptx.cuh", "attn_common.cuh", "attn_fwd_serial.cuh", "attn_fwd_ws.cuh", "thd_attn.cu",
+                   "padding_mask.cu")]
+
+
+def effective_flops(w):
+    """4 * d * Hq per unmasked (query, key) pair: QK^T and PV, multiply-adds counted as 2."""
+    L = w.lengths.astype(np.float64)
+    pairs = np.where(w.causal, L * (L + 1) / 2, L * L).sum()
+    return 4.0 * w.head_dim * w.num_heads_q * pairs
+
+
+def attn_bytes(w):
+    """Algorithmic HBM bytes of one attention launch: Q, K, V read once, O and LSE written once."""
+    T, e = w.total_tokens, 2
+    return T * (2 * w.num_heads_q + 2 * w.num_heads_kv) * w.head_dim * e + T * w.num_heads_q * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        path = os.path.join(ROOT, rel)
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, _, v = line.partition(":")
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.result = self._finish()
+
+    def _finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+# oracle on host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------------------------
+
+def oracle_sample(w, budget_s):
+    """Time the fp64 oracle on whole query-row blocks of the workload until `budget_s` elapses.
+
+    Returns (effective FLOP/s, description)."""
+    import oracle
+    group = w.num_heads_q // w.num_heads_kv
+    done_pairs = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    blocks = []
+    for b in np.argsort(-w.lengths):
+        L = int(w.lengths[b])
+        for r0 in range(0, L, 512):
+            blocks.append((int(b), r0, min(L, r0 + 512)))
+    rng = np.random.default_rng(0)
+    rng.shuffle(blocks)
+    it = 0
+    while time.perf_counter() - t0 < budget_s and it < len(blocks):
+        b, r0, r1 = blocks[it]
+        h = it % w.num_heads_q
+        it += 1
+        s, L = int(w.starts[b]), int(w.lengths[b])
+        rows = np.arange(r0, r1)
+        oracle.thd_attention_rows(w.q, w.k, w.v, s, s, L, bool(w.causal[b]), h, group, w.softmax_scale, rows)
+        done_pairs += float((rows + 1).sum()) if w.causal[b] else float(len(rows) * L)
+        rows_done += len(rows)
+    el = time.perf_counter() - t0
+    flops = 4.0 * w.head_dim * done_pairs
+    desc = (f"{it} blocks of <=512 query rows (one head each) drawn from {w.name}: {rows_done} rows, "
+            f"{done_pairs:.3e} unmasked pairs, {el:.1f} s")
+    return flops / el, desc, el
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    w = workloads.make(WORKLOAD)
+    eff = effective_flops(w)
+    per_step = []
+    descs = []
+    budget = min(args.ref_budget, 150.0 / (args.warmup + args.steps))
+    for i in range(args.warmup + args.steps):
+        rate, desc, el = oracle_sample(w, budget)
+        if i >= args.warmup:
+            per_step.append(rate)
+            descs.append(desc)
+    rate = statistics.median(per_step)
+    value = rate / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": eff / rate * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _NCORES, "kind": "oracle",
+                         "sample": descs[-1]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "fp64 numpy oracle on host cores; each step times a bounded sample of the workload and "
+                "ms_per_step extrapolates that rate to the whole batch",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: {w.batch_size} packed sequences, {w.total_tokens} tokens, "
+                        f"{int(w.causal.sum())} causal / {int((~w.causal).sum())} full, no gaps, "
+                        f"metadata buffers sized for {len(w.cu_seqlens) - 1} sequences",
+            "batch": w.batch_size, "total_tokens": w.total_tokens, "heads_q": w.num_heads_q,
+            "heads_kv": w.num_heads_kv, "head_dim": w.head_dim,
+            "lengths": [int(x) for x in w.lengths], "causal": [bool(x) for x in w.causal],
+            "mask_step": {"batch": w.batch_size, "max_seqlen": int(w.max_seqlen)},
+            "l2": "inputs larger than L2 (Q/K/V 1.5 GB per step), no flush needed",
+            "parallelism": "one replica per GPU"}
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+
+def run_gpu(args, ws, rank, local):
+    import variable_length_packed_gb300 as vlp
+    from variable_length_packed_gb300 import build as vbuild
+
+    vbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    w = workloads.make(WORKLOAD)
+    eff = effective_flops(w)
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    causal = torch.from_numpy(w.seq_is_causal).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.num_heads_q, w.total_tokens), dtype=torch.float32, device=dev)
+    wsp = torch.zeros(vlp.thd_attn_workspace_size(), dtype=torch.uint8, device=dev)
+    S = int(w.max_seqlen)
+    mask = torch.empty((w.batch_size, 1, 1, S), dtype=torch.bool, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        vlp.thd_attn_fwd(q, k, v, cu, cu, None, None, causal, w.batch_size, S, w.softmax_scale, out=out,
+                         lse=lse, workspace=wsp)
+        if ev is not None:
+            ev[1].record(stream)
+        vlp.thd_padding_mask(cu, w.batch_size, S, mask=mask)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = int(wsp[8:12].cpu().numpy().view(np.uint32)[0])
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = ws * eff / (ms_per_step * 1e-3) / 1e12
+
+    # ---- padding mask alone on the 4096 x 8192 workload (CUDA graph of back-to-back launches) ----
+    mw = workloads.make_mask()
+    mcu = torch.from_numpy(mw.cu_seqlens).to(dev)
+    mmask = torch.empty((mw.batch_size, 1, 1, mw.max_seqlen), dtype=torch.bool, device=dev)
+    for _ in range(3):
+        vlp.thd_padding_mask(mcu, mw.batch_size, mw.max_seqlen, mask=mmask)
+    torch.cuda.synchronize()
+    reps = 200
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream(dev)
+    s2.wait_stream(stream)
+    with torch.cuda.stream(s2):
+        with torch.cuda.graph(g, stream=s2):
+            for _ in range(reps):
+                vlp.thd_padding_mask(mcu, mw.batch_size, mw.max_seqlen, mask=mmask)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record(stream)
+    g.replay()
+    m1.record(stream)
+    torch.cuda.synchronize()
+    mask_us = m0.elapsed_time(m1) * 1e3 / reps
+    mask_bytes = mw.batch_size * mw.max_seqlen + 4 * (mw.batch_size + 1)
+    mask_gbs = mask_bytes / (mask_us * 1e-6) / 1e9
+
+    # ---- end to end through the public API with host buffers ----
+    hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
+    hcu = torch.from_numpy(w.cu_seqlens).pin_memory()
+    hcausal = torch.from_numpy(w.seq_is_causal).pin_memory()
+    hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    hlse = torch.empty((w.num_heads_q, w.total_tokens), dtype=torch.float32).pin_memory()
+    hmask = torch.empty((w.batch_size, 1, 1, S), dtype=torch.bool).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        cu.copy_(hcu, non_blocking=True)
+        causal.copy_(hcausal, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hmask.copy_(mask, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, ws, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcu, hcausal))
+    d2h = sum(t.numel() * t.element_size() for t in (hout, hlse, hmask))
+
+    # ---- check the timed output once against the oracle on a few rows (not timed) ----
+    import oracle
+    rows = np.array([0, 1, 1000, int(w.lengths[0]) - 1])
+    ro, rl = oracle.thd_attention_rows(w.q, w.k, w.v, 0, 0, int(w.lengths[0]), bool(w.causal[0]), 0, 1,
+                                       w.softmax_scale, rows)
+    got = out[torch.from_numpy(rows).to(dev), 0].float().cpu().double().numpy()
+    check_err = float(np.abs(got - ro).max())
+
+    achieved = eff / (attn_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+        "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": recorded_traffic("attn_fwd"),
+                     "kernel": "thd attention forward", "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "frac_of_sustained_peak": achieved / peaks["bf16_tflops_sustained"],
+                     "attn_ms_per_launch": attn_ms, "algorithmic_flops_per_launch": eff,
+                     "algorithmic_bytes_per_launch": attn_bytes(w)},
+        "mask": {"workload": "mask_many: batch 4096, max_seqlen 8192, lengths U{0..8192}",
+                 "us_per_launch": mask_us, "gbs": mask_gbs, "peak_gbs": peaks["hbm_gbs"],
+                 "frac": mask_gbs / peaks["hbm_gbs"], "algorithmic_bytes": mask_bytes,
+                 "timing": f"CUDA graph of {reps} back-to-back launches", "traffic": recorded_traffic("padding_mask")},
+        "e2e": {"value": ws * eff / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.result,
+        "device_status_word": status,
+        "sampled_check_max_abs_err": check_err,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc, el = oracle_sample(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": _NCORES, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    return run_gpu(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,134 @@
+/*
+ * thd_attn.h — C ABI of libthdattn.so: forward self-attention over packed
+ * variable-length (THD) tensors, and the attention padding mask, on one
+ * NVIDIA GB300 (sm_103a) GPU.
+ *
+ * Every pointer argument named "device" is a CUDA device pointer; the library
+ * never dereferences it on the host and never synchronises the stream, so the
+ * calls are asynchronous and may be captured in a CUDA graph.  `stream` is a
+ * cudaStream_t passed as void* (NULL = the legacy default stream).  The caller
+ * owns every buffer.  The library allocates no device memory.
+ *
+ * Return values are thd_status codes.  Arguments that can be checked on the
+ * host are checked before anything is launched; nothing is launched when a
+ * check fails.  Device metadata (cu_seqlens*, seq_is_causal) is never read on
+ * the host: invalid device metadata gives unspecified output, but every
+ * address the kernels form is clamped to the buffers described by the host
+ * arguments, so it does not fault.
+ */
+#ifndef THD_ATTN_H
+#define THD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  THD_OK = 0,
+  THD_ERR_ARG = -1,          /* a host-checkable argument is invalid                */
+  THD_ERR_UNSUPPORTED = -2,  /* valid but not supported (head_dim, dtype, heads)    */
+  THD_ERR_CUDA = -3,         /* a CUDA runtime / driver call failed                  */
+  THD_ERR_WORKSPACE = -4     /* workspace missing, too small or misaligned          */
+} thd_status;
+
+typedef enum { THD_BF16 = 0, THD_FP16 = 1 } thd_dtype;
+
+/* Bits of the device status word (workspace byte offset 8, uint32). */
+#define THD_STATUS_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up; output unspecified */
+
+/*
+ * thd_attn_workspace_size — bytes of device workspace thd_attn_fwd needs.
+ *
+ * The workspace holds the dynamic tile scheduler's work counter (uint64 at
+ * byte 0) and the device status word (uint32 at byte 8, THD_STATUS_* bits).
+ * thd_attn_fwd clears both on `stream` before its kernel starts, so the
+ * workspace needs no initialisation, but two calls that share one workspace
+ * must not overlap on the GPU.  Alignment: 16 bytes.
+ */
+size_t thd_attn_workspace_size(void);
+
+/*
+ * thd_attn_fwd — softmax(scale * Q K^T [+ causal mask]) V per packed sequence,
+ * with a per-sequence causal/full policy, all sequences in one kernel launch.
+ *
+ * Sources: THD layout and cu_seqlens — "How to pad sequences that cannot be
+ * evenly split in context parallelism (CP)?" (Megatron-LM issue, repro
+ * script); per-sequence policy `thd_sequence_is_causal` and the padded-slot
+ * arrays cu_seqlens_*_padded — "Add per-sequence causal policy to packed THD
+ * attention" (TransformerEngine PR, Changes and the pad_between_seqs review
+ * comment); buffers longer than batch_size + 1 — "[PyTorch] Build the
+ * attention padding mask without host syncs" (Changes).
+ *
+ * q            device, [T, Hq, head_dim] contiguous, dtype, 16-byte aligned.
+ * k, v         device, [T, Hkv, head_dim] contiguous, dtype, 16-byte aligned.
+ * cu_seqlens_q, cu_seqlens_kv
+ *              device int32, >= batch_size + 1 entries; entry b+1 minus entry b
+ *              is sequence b's valid length.  Entries past batch_size are
+ *              never read.
+ * cu_seqlens_q_padded, cu_seqlens_kv_padded
+ *              device int32 or NULL.  Entry b is the first row of sequence b's
+ *              slot in the packed buffer; the slot's first `length` rows are
+ *              valid and the rest, up to the next slot, are pad.  NULL means
+ *              sequence b starts at cu_seqlens[b] (no gaps).  Entries past
+ *              batch_size - 1 are never read.
+ * seq_is_causal device uint8 [>= batch_size] or NULL (all full-context).  Non-zero
+ *              selects top-left causal masking (key j visible to query i iff
+ *              j <= i, positions counted from the sequence's first token).
+ * batch_size   >= 0.  0 writes zeros to every row of `out` (and -inf to lse).
+ * max_seqlen   >= 0; a sizing hint only (the kernels read the true lengths).
+ * softmax_scale finite, > 0.
+ * out          device, [T, Hq, head_dim], dtype.  Rows of no sequence (gaps,
+ *              leading and trailing pad) are written as exact zeros.
+ * lse          device float32 [Hq, T] or NULL.  Natural-log log-sum-exp of the
+ *              scaled logits of each valid row; -inf on pad rows.
+ * total_tokens T >= 0 (rows of q/k/v/out).
+ * num_heads_q, num_heads_kv  Hq >= 1, Hkv >= 1, Hq % Hkv == 0; query head h reads
+ *              key/value head h / (Hq / Hkv).
+ * head_dim     a multiple of 8 in [8, 128].
+ * dtype        thd_dtype (bf16 or fp16); fp32 accumulation, output rounded to
+ *              nearest even.
+ * workspace    device, >= thd_attn_workspace_size() bytes, 16-byte aligned.
+ * stream       cudaStream_t.
+ *
+ * Errors: THD_ERR_ARG (bad sizes, NULL required pointer, misalignment),
+ * THD_ERR_UNSUPPORTED (head_dim, Hq % Hkv), THD_ERR_WORKSPACE, THD_ERR_CUDA.
+ */
+int thd_attn_fwd(const void* q, const void* k, const void* v,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                 const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                 const uint8_t* seq_is_causal,
+                 int batch_size, int max_seqlen, float softmax_scale,
+                 void* out, float* lse,
+                 int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                 int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * thd_padding_mask — the boolean attention padding mask built on the device,
+ * mask[b, p] = (p >= cu_seqlens[b+1] - cu_seqlens[b]) for b < batch_size,
+ * p < max_seqlen (1 = padded position).
+ *
+ * Source: "[PyTorch] Build the attention padding mask without host syncs"
+ * (TransformerEngine PR): the vectorised form (Description), the
+ * [1 : batch_size + 1] slice that ignores longer buffers (Changes), and the
+ * all-False row of a sequence longer than max_seqlen (Equivalence).
+ *
+ * cu_seqlens   device int32, >= batch_size + 1 entries (only those are read).
+ * batch_size   >= 0;  max_seqlen >= 0.  Either 0: nothing is launched.
+ * mask         device uint8 [batch_size * max_seqlen] (the [B, 1, 1, S] bool
+ *              tensor's bytes), any alignment; every byte is written 0 or 1.
+ * Errors: THD_ERR_ARG (negative sizes, NULL pointers, B*S overflow), THD_ERR_CUDA.
+ */
+int thd_padding_mask(const int32_t* cu_seqlens, int batch_size, int max_seqlen,
+                     uint8_t* mask, void* stream);
+
+/* Human-readable name of a thd_status value (static storage). */
+const char* thd_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* THD_ATTN_H */

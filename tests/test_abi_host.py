@@ -1,0 +1,93 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the header
+declares, and rejects invalid host arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+pytest.importorskip("torch")
+import variable_length_packed_gb300 as vlp  # noqa: E402
+from variable_length_packed_gb300 import build as vbuild  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lib():
+    vbuild.build()
+    return vlp.load_library()
+
+
+def header_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(thd_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert {"thd_attn_fwd", "thd_padding_mask", "thd_attn_workspace_size", "thd_status_string"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_workspace(lib):
+    assert vlp.thd_attn_workspace_size() >= 16
+    for s in (0, -1, -2, -3, -4):
+        assert vlp.thd_status_string(s).startswith("THD_")
+
+
+def call_fwd(lib, **over):
+    args = dict(q=16, k=16, v=16, cu_q=16, cu_kv=16, pq=None, pkv=None, causal=None, B=1, S=8, scale=0.125,
+                out=16, lse=None, T=8, Hq=2, Hkv=2, d=64, dtype=0, ws=16, ws_bytes=256, stream=None)
+    args.update(over)
+    P = ctypes.c_void_p
+    return lib.thd_attn_fwd(P(args["q"]), P(args["k"]), P(args["v"]), P(args["cu_q"]), P(args["cu_kv"]),
+                            P(args["pq"]), P(args["pkv"]), P(args["causal"]), args["B"], args["S"],
+                            args["scale"], P(args["out"]), P(args["lse"]), args["T"], args["Hq"],
+                            args["Hkv"], args["d"], args["dtype"], P(args["ws"]), args["ws_bytes"],
+                            P(args["stream"]))
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(B=-1), -1), (dict(T=-1), -1), (dict(S=-1), -1), (dict(Hq=0), -1), (dict(Hkv=0), -1),
+    (dict(scale=float("nan")), -1), (dict(scale=0.0), -1), (dict(scale=-1.0), -1),
+    (dict(scale=float("inf")), -1), (dict(dtype=7), -2), (dict(d=4), -2), (dict(d=136), -2),
+    (dict(d=60), -2), (dict(Hq=3, Hkv=2), -2), (dict(q=None), -1), (dict(out=None), -1),
+    (dict(cu_q=None), -1), (dict(q=24), -1), (dict(out=12), -1), (dict(lse=6), -1),
+    (dict(ws=None), -4), (dict(ws=8), -4), (dict(ws_bytes=8), -4),
+    (dict(T=2**31 - 1, Hq=256, Hkv=256), -2),
+])
+def test_invalid_arguments_rejected_before_launch(lib, over, status):
+    assert call_fwd(lib, **over) == status
+
+
+def test_trivial_calls_launch_nothing(lib):
+    # no rows: nothing to write, returns OK without any CUDA call (works without a GPU)
+    assert call_fwd(lib, T=0, q=None, k=None, v=None, out=None) == 0
+    P = ctypes.c_void_p
+    assert lib.thd_padding_mask(P(None), 0, 8, P(None), P(None)) == 0
+    assert lib.thd_padding_mask(P(16), 4, 0, P(16), P(None)) == 0
+    assert lib.thd_padding_mask(P(16), -1, 8, P(16), P(None)) == -1
+    assert lib.thd_padding_mask(P(16), 4, -2, P(16), P(None)) == -1
+    assert lib.thd_padding_mask(P(None), 4, 8, P(16), P(None)) == -1
+    assert lib.thd_padding_mask(P(16), 4, 8, P(None), P(None)) == -1
+    assert lib.thd_padding_mask(P(18), 4, 8, P(16), P(None)) == -1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(TypeError):
+        vlp.thd_attn_fwd(x, x, x, cu, cu)
+    with pytest.raises(TypeError):
+        vlp.thd_padding_mask(cu, 1, 4)

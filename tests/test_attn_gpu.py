@@ -1,0 +1,203 @@
+"""thd_attn_fwd on the GPU against the fp64 oracle, element by element.
+
+Small workloads are compared on every row; the large ones (mixed-policy GQA, long
+context, many short sequences) on sampled (sequence, head, row) triples computed one by
+one by the oracle, plus every pad row (exact zero / -inf LSE).  Tolerances: |out| 1e-2
+for bf16 inputs, 2e-3 for fp16, |LSE| 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from conftest import read_golden
+from thd_testutil import (boundary_rows, check_pad_rows, compare_full, compare_sampled, run_gpu,
+                          to_device, valid_rows)
+
+pytestmark = pytest.mark.gpu
+vlp = pytest.importorskip("variable_length_packed_gb300")
+
+
+def status_word(ws):
+    return int(ws[8:12].cpu().numpy().view(np.uint32)[0])
+
+
+def workspace():
+    return torch.zeros(vlp.thd_attn_workspace_size(), dtype=torch.uint8, device="cuda")
+
+
+# --- small workloads: every row -------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["page1", "page1_pad", "tiny_mixed", "padded_gaps"])
+def test_small_workloads_every_row(name):
+    w = workloads.make(name)
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws)
+    assert status_word(ws) == 0
+    compare_full(w, out, lse)
+
+
+def test_page1_printed_values_on_gpu():
+    g = read_golden("page1_full_attention.txt")
+    for name in ("page1", "page1_pad"):
+        w = workloads.make(name)
+        out, lse = run_gpu(w)
+        o = out.float().cpu().numpy()
+        for r in range(7):
+            assert np.all(np.abs(o[r, 0] - float(g[f"row {r}"])) <= 0.5e-4), (name, r, o[r, 0])
+        if name == "page1_pad":
+            assert np.all(o[7] == 0.0) and torch.isneginf(lse[0, 7])
+
+
+def test_two_call_identity_on_gpu():
+    """out(causal call) + out(full call) with the page's arrays equals the mixed-policy call."""
+    g = read_golden("page2_two_call.txt")
+    w = workloads.make("tiny_mixed")
+    dev = to_device(w)
+    ints = lambda key: torch.tensor([int(t) for t in g[key].split()], dtype=torch.int32, device="cuda")
+    out_c, lse_c = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], ints("causal_call.cu_seqlens"),
+                                    ints("causal_call.cu_seqlens"), ints("causal_call.cu_seqlens_padded"),
+                                    ints("causal_call.cu_seqlens_padded"),
+                                    torch.ones(4, dtype=torch.bool, device="cuda"), 4, 3, w.softmax_scale)
+    out_f, lse_f = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], ints("full_call.cu_seqlens"),
+                                    ints("full_call.cu_seqlens"), ints("full_call.cu_seqlens_padded"),
+                                    ints("full_call.cu_seqlens_padded"), None, 3, 4, w.softmax_scale)
+    out, lse = run_gpu(w, dev=dev)
+    torch.cuda.synchronize()
+    # each row is computed by the same tile arithmetic in both forms: equal bit for bit
+    assert torch.equal(out_c + out_f, out)
+    assert torch.equal(torch.logaddexp(lse_c, lse_f), lse)
+    compare_full(w, out, lse)
+
+
+# --- large workloads: sampled rows ----------------------------------------------------------
+
+def test_mixed_gqa_sampled():
+    w = workloads.make("mixed_gqa")
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws)
+    assert status_word(ws) == 0
+    rng = np.random.default_rng(20)
+    order = np.argsort(-w.lengths)
+    seqs = list(order[:3]) + list(rng.choice(w.batch_size, size=5, replace=False))
+    pairs = [(int(b), int(h)) for b in seqs for h in rng.choice(w.num_heads_q, size=3, replace=False)]
+    compare_sampled(w, out, lse, pairs, lambda L: boundary_rows(L, rng, extra=24))
+
+
+def test_long_context_sampled():
+    w = workloads.make("long_context")
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws)
+    assert status_word(ws) == 0
+    rng = np.random.default_rng(30)
+    pairs = [(b, int(h)) for b in range(w.batch_size) for h in rng.choice(w.num_heads_q, size=2, replace=False)]
+    compare_sampled(w, out, lse, pairs, lambda L: boundary_rows(L, rng, extra=16))
+
+
+def test_many_short_sampled():
+    w = workloads.make("many_short")
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws)
+    assert status_word(ws) == 0
+    rng = np.random.default_rng(40)
+    seqs = rng.choice(w.batch_size, size=150, replace=False)
+    pairs = [(int(b), int(h)) for b in seqs for h in rng.choice(w.num_heads_q, size=4, replace=False)]
+    compare_sampled(w, out, lse, pairs, lambda L: np.arange(L))
+
+
+# --- edge cases -----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,dtype", [(8, torch.float16), (16, torch.bfloat16), (32, torch.float16),
+                                     (40, torch.bfloat16), (64, torch.float16), (72, torch.bfloat16),
+                                     (96, torch.float16), (128, torch.float16), (128, torch.bfloat16)])
+def test_head_dims_and_tile_boundaries(d, dtype):
+    lens = [1, 127, 128, 129, 255, 256, 257, 3]
+    causal = [1, 0, 1, 0, 1, 0, 1, 1]
+    w = workloads.from_lengths(f"edge_d{d}", lens, causal, gaps_before=[5, 0, 1, 7, 0, 64, 2, 9], trailing=3,
+                               heads_q=4, heads_kv=2, head_dim=d, dtype=dtype, seed=d)
+    out, lse = run_gpu(w)
+    compare_full(w, out, lse)
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_gqa_groups(group):
+    w = workloads.from_lengths("gqa", [200, 77, 300], [1, 0, 1], gaps_before=[0, 3, 1], heads_q=8,
+                               heads_kv=8 // group, head_dim=64, dtype=torch.bfloat16, seed=group)
+    out, lse = run_gpu(w)
+    compare_full(w, out, lse)
+
+
+def test_empty_batch_zeroes_everything():
+    w = workloads.make("tiny_mixed")
+    dev = to_device(w)
+    out = torch.full_like(dev["q"], 7.0)
+    lse = torch.zeros((w.num_heads_q, w.total_tokens), dtype=torch.float32, device="cuda")
+    vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], batch_size=0, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_zero_length_sequences_and_lse_optional():
+    w = workloads.from_lengths("zeros", [5, 0, 7, 0, 130], [1, 1, 0, 0, 1], gaps_before=[0, 2, 0, 4, 1],
+                               heads_q=2, head_dim=64, dtype=torch.bfloat16, seed=8, with_padded=True)
+    out, lse = run_gpu(w)
+    compare_full(w, out, lse)
+    out2, lse2 = run_gpu(w, return_lse=False)
+    assert lse2 is None and torch.equal(out2, out)
+
+
+def test_gap_contents_do_not_leak():
+    outs = []
+    for fill in (100.0, -1e4, 0.0):
+        w = workloads.from_lengths("leak", [100, 300, 31], [1, 0, 1], gaps_before=[17, 64, 3], trailing=9,
+                                   heads_q=2, head_dim=128, dtype=torch.bfloat16, seed=12, gap_fill=fill)
+        out, lse = run_gpu(w)
+        vr = torch.from_numpy(valid_rows(w)).cuda()
+        outs.append((out[vr], lse[:, vr]))
+        check_pad_rows(w, out, lse)
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_garbage_past_batch_is_ignored_and_deterministic():
+    w = workloads.from_lengths("tail", [50, 260, 9], [0, 1, 1], heads_q=2, head_dim=64, dtype=torch.float16,
+                               seed=13, capacity=16, rng=np.random.default_rng(5))
+    out1, lse1 = run_gpu(w)
+    out2, lse2 = run_gpu(w)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    compare_full(w, out1, lse1)
+
+
+def test_writes_stay_inside_out_and_lse():
+    w = workloads.from_lengths("guard", [33, 140], [1, 0], gaps_before=[2, 5], trailing=4, heads_q=2,
+                               head_dim=64, dtype=torch.bfloat16, seed=14)
+    dev = to_device(w)
+    T, H, d = w.total_tokens, w.num_heads_q, w.head_dim
+    g = 64
+    obuf = torch.full((T + 2 * g, H, d), 3.0, dtype=w.dtype, device="cuda")
+    lbuf = torch.full((H * T + 2 * 1024,), 5.0, dtype=torch.float32, device="cuda")
+    out = obuf[g:g + T]
+    lse = lbuf[1024:1024 + H * T].view(H, T)
+    vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"], dev["padded"],
+                     dev["causal"], w.batch_size, w.max_seqlen, w.softmax_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(obuf[:g] == 3.0) and torch.all(obuf[g + T:] == 3.0)
+    assert torch.all(lbuf[:1024] == 5.0) and torch.all(lbuf[1024 + H * T:] == 5.0)
+    compare_full(w, out, lse)
+
+
+def test_non_monotone_metadata_does_not_fault():
+    """Invalid device metadata: unspecified output, but the call completes without a fault."""
+    w = workloads.from_lengths("bad", [40, 40, 40], [1, 0, 1], heads_q=2, head_dim=64, dtype=torch.bfloat16,
+                               seed=15)
+    dev = to_device(w)
+    bad_cu = torch.tensor([0, 100, 20, 10000], dtype=torch.int32, device="cuda")
+    bad_pad = torch.tensor([-50, 90, 119, 3], dtype=torch.int32, device="cuda")
+    ws = workspace()
+    vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], bad_cu, bad_cu, bad_pad, bad_pad, dev["causal"], 3, 40,
+                     0.125, workspace=ws)
+    torch.cuda.synchronize()
+    assert status_word(ws) == 0

@@ -1,0 +1,97 @@
+"""Helpers shared by the GPU parity tests: move a workload to the device, call the library,
+compare with the fp64 oracle at the stated tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import variable_length_packed_gb300 as vlp
+
+# Acceptance bounds: output absolute error 1e-2 (bf16 inputs) / 2e-3 (fp16 inputs),
+# LSE absolute error 1e-3; pad rows and the mask bit-exact.
+OUT_ATOL = {torch.bfloat16: 1e-2, torch.float16: 2e-3}
+LSE_ATOL = 1e-3
+
+
+def to_device(w, device="cuda"):
+    dev = torch.device(device)
+    d = dict(
+        q=w.q.to(dev), k=w.k.to(dev), v=w.v.to(dev),
+        cu=torch.from_numpy(w.cu_seqlens).to(dev),
+        padded=None if w.cu_seqlens_padded is None else torch.from_numpy(w.cu_seqlens_padded).to(dev),
+        causal=torch.from_numpy(w.seq_is_causal).to(dev),
+    )
+    return d
+
+
+def run_gpu(w, dev=None, workspace=None, **over):
+    dev = dev or to_device(w)
+    args = dict(cu_seqlens_q_padded=dev["padded"], cu_seqlens_kv_padded=dev["padded"],
+                seq_is_causal=dev["causal"], batch_size=w.batch_size, max_seqlen=w.max_seqlen,
+                softmax_scale=w.softmax_scale, workspace=workspace)
+    args.update(over)
+    out, lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], **args)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def valid_rows(w):
+    m = np.zeros(w.total_tokens, dtype=bool)
+    for s, L in zip(w.starts, w.lengths):
+        m[int(s):int(s) + int(L)] = True
+    return m
+
+
+def check_pad_rows(w, out, lse):
+    """Rows of no sequence: exact zeros, LSE exactly -inf."""
+    pad = torch.from_numpy(~valid_rows(w)).to(out.device)
+    if pad.any():
+        assert torch.all(out[pad] == 0), "pad rows not exact zero"
+        if lse is not None:
+            assert torch.all(torch.isneginf(lse[:, pad])), "pad LSE not -inf"
+
+
+def compare_full(w, out, lse, ref_out=None, ref_lse=None):
+    """Element-wise comparison of every row against the whole-batch oracle."""
+    if ref_out is None:
+        ref_out, ref_lse = oracle.thd_attention_fwd(
+            w.q, w.k, w.v, w.cu_seqlens, w.cu_seqlens, w.cu_seqlens_padded, w.cu_seqlens_padded,
+            w.seq_is_causal, w.batch_size, w.softmax_scale)
+    o = out.float().cpu().double().numpy()
+    vr = valid_rows(w)
+    err = np.abs(o[vr] - ref_out[vr])
+    tol = OUT_ATOL[w.dtype]
+    assert err.max(initial=0.0) <= tol, f"{w.name}: max |out err| {err.max():.3e} > {tol}"
+    if lse is not None:
+        l = lse.cpu().double().numpy()
+        lerr = np.abs(l[:, vr] - ref_lse[:, vr])
+        assert lerr.max(initial=0.0) <= LSE_ATOL, f"{w.name}: max |lse err| {lerr.max():.3e}"
+    check_pad_rows(w, out, lse)
+    return float(err.max(initial=0.0))
+
+
+def compare_sampled(w, out, lse, pairs, rows_for):
+    """Compare selected rows of selected (sequence, head) pairs against the oracle, row by row."""
+    group = w.num_heads_q // w.num_heads_kv
+    worst = 0.0
+    for b, h in pairs:
+        s, L = int(w.starts[b]), int(w.lengths[b])
+        rows = np.unique(np.clip(np.asarray(rows_for(L)), 0, L - 1))
+        ref_o, ref_l = oracle.thd_attention_rows(w.q, w.k, w.v, s, s, L, bool(w.causal[b]), h, group,
+                                                 w.softmax_scale, rows)
+        got = out[s + torch.from_numpy(rows).to(out.device), h, :].float().cpu().double().numpy()
+        err = np.abs(got - ref_o).max()
+        assert err <= OUT_ATOL[w.dtype], f"{w.name} b={b} h={h}: |out err| {err:.3e}"
+        if lse is not None:
+            gl = lse[h, s + torch.from_numpy(rows).to(lse.device)].cpu().double().numpy()
+            lerr = np.abs(gl - ref_l).max()
+            assert lerr <= LSE_ATOL, f"{w.name} b={b} h={h}: |lse err| {lerr:.3e}"
+        worst = max(worst, float(err))
+    check_pad_rows(w, out, lse)
+    return worst
+
+
+def boundary_rows(L, rng, extra=6):
+    base = [0, 1, 2, 63, 64, 127, 128, 129, 255, 256, L // 2, L - 2, L - 1]
+    return base + list(rng.integers(0, L, size=extra))

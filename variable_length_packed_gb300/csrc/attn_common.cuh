@@ -1,0 +1,299 @@
+// attn_common.cuh — parameters, sequence metadata decoding, the in-kernel
+// varlen tile scheduler and pad-row zeroing shared by the attention kernels.
+//
+// Semantics (web pages; titles and sections):
+//  * "How to pad sequences that cannot be evenly split in context parallelism
+//    (CP)?" (Megatron-LM issue, repro script): THD layout [t, h, d], sequence
+//    boundaries from cu_seqlens.
+//  * "Add per-sequence causal policy to packed THD attention"
+//    (TransformerEngine PR, Changes; pad_between_seqs review comment): one
+//    causal flag per sequence; cu_seqlens_padded gives each sequence's slot
+//    start, the rows of a slot past its valid length are padding, and padding
+//    rows of the output are zero.
+//  * "[PyTorch] Build the attention padding mask without host syncs"
+//    (TransformerEngine PR, Changes): metadata buffers may be longer than
+//    batch_size + 1; only the first batch_size + 1 entries are read.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace thd {
+
+constexpr int kBlockN = 128;            // keys per KV tile
+constexpr int kTileM = 128;             // query rows per Q tile (UMMA M)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint32_t THD_WAIT_TIMEOUT_BIT = 1u;     // device status bit of a timed-out wait
+
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  const int32_t* pad_q;    // may be null
+  const int32_t* pad_kv;   // may be null
+  const uint8_t* causal;   // may be null
+  void* out;
+  float* lse;              // may be null
+  unsigned long long* work_counter;
+  uint32_t* status;
+  int B, T, Hq, Hkv, d, group;
+  float scale;             // softmax scale
+  float scale_log2;        // softmax scale * log2(e)
+};
+
+struct SeqInfo {
+  int q_start, kv_start, q_len, kv_len, causal;
+};
+
+// Sequence b's rows, clamped to the packed buffer [0, T): garbage metadata
+// gives garbage output but never an out-of-range address.
+__device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
+  SeqInfo s;
+  const long long cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1];
+  const long long ck0 = p.cu_kv[b], ck1 = p.cu_kv[b + 1];
+  long long qs = p.pad_q ? (long long)p.pad_q[b] : cq0;
+  long long ks = p.pad_kv ? (long long)p.pad_kv[b] : ck0;
+  long long ql = cq1 - cq0, kl = ck1 - ck0;
+  qs = qs < 0 ? 0 : (qs > p.T ? p.T : qs);
+  ks = ks < 0 ? 0 : (ks > p.T ? p.T : ks);
+  ql = ql < 0 ? 0 : (ql > p.T - qs ? p.T - qs : ql);
+  kl = kl < 0 ? 0 : (kl > p.T - ks ? p.T - ks : kl);
+  s.q_start = (int)qs;
+  s.kv_start = (int)ks;
+  s.q_len = (int)ql;
+  s.kv_len = (int)kl;
+  s.causal = p.causal ? (p.causal[b] != 0) : 0;
+  return s;
+}
+
+// Number of KV tiles a Q tile whose first row is sequence position q0 must
+// visit: all keys for a full-context sequence, keys up to the tile's last
+// valid row for a causal one (top-left alignment: key j visible iff j <= i).
+__device__ __forceinline__ int kv_tiles_for(const SeqInfo& s, int q0, int rows) {
+  if (s.kv_len <= 0) return 0;
+  int last = s.kv_len - 1;
+  if (s.causal) {
+    int qlast = min(q0 + rows, s.q_len) - 1;
+    last = min(last, qlast);
+    if (last < 0) return 0;
+  }
+  return last / kBlockN + 1;
+}
+
+// ----------------------------------------------------------------------------
+// Tile scheduler.  Work item = (sequence, query head, block of BLOCK_M query
+// rows).  Sequences are taken in chunks of kSchedChunk (in batch order); inside
+// a chunk they are ordered longest first (counting sort on the number of KV
+// tiles, full-context before causal at equal length), each sequence's items
+// run head by head with its heaviest (last) query block first.  CTAs claim
+// items from one global counter, so the order above is the order in which
+// work starts (longest-processing-time-first list scheduling).  Pad gaps
+// produce no items; fully masked causal tiles are never visited because each
+// block only loops over kv_tiles_for() tiles.  Each CTA rebuilds the same
+// chunk order in its shared memory from the device metadata, so no host
+// synchronisation and no second launch are needed.
+// ----------------------------------------------------------------------------
+constexpr int kSchedChunk = 1024;
+constexpr int kSchedBuckets = 1024;
+
+struct SchedSmem {
+  uint32_t off[kSchedBuckets];      // histogram, then running bucket offsets
+  uint32_t cum[kSchedChunk + 1];    // exclusive prefix of item counts, sorted order
+  uint16_t key[kSchedChunk];        // sort key per chunk-local sequence
+  uint16_t order[kSchedChunk];      // chunk-local sequence ids, sorted
+  int chunk_base;
+  int chunk_n;
+  unsigned long long item_base;
+  unsigned long long item_end;
+};
+
+__device__ __forceinline__ uint32_t seq_sort_key(const SeqInfo& s) {
+  int nkv = (s.kv_len + kBlockN - 1) / kBlockN;
+  nkv = nkv > 511 ? 511 : nkv;
+  return (uint32_t)(nkv * 2 + (s.causal ? 0 : 1));
+}
+
+template <int BLOCK_M>
+__device__ __forceinline__ uint32_t seq_items(const SeqInfo& s, int Hq) {
+  return s.q_len > 0 ? (uint32_t)((s.q_len + BLOCK_M - 1) / BLOCK_M) * (uint32_t)Hq : 0u;
+}
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Load and sort the chunk of sequences starting at `base`.  One full warp.
+template <int BLOCK_M>
+__device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
+  const int lane = threadIdx.x & 31;
+  const int n = min(kSchedChunk, p.B - base);
+  for (int i = lane; i < kSchedBuckets; i += 32) s.off[i] = 0u;
+  __syncwarp();
+  for (int i = lane; i < n; i += 32) {
+    uint32_t k = seq_sort_key(load_seq(p, base + i));
+    s.key[i] = (uint16_t)k;
+    atomicAdd(&s.off[k], 1u);
+  }
+  __syncwarp();
+  // exclusive offsets, keys in descending order; lane l owns 32 consecutive keys
+  uint32_t sum = 0;
+  for (int t = 0; t < 32; ++t) sum += s.off[kSchedBuckets - 1 - (lane * 32 + t)];
+  uint32_t run = warp_incl_scan(sum) - sum;
+  __syncwarp();
+  for (int t = 0; t < 32; ++t) {
+    const int kidx = kSchedBuckets - 1 - (lane * 32 + t);
+    const uint32_t c = s.off[kidx];
+    s.off[kidx] = run;
+    run += c;
+  }
+  __syncwarp();
+  // stable scatter: 32 sequences at a time, equal keys ranked by lane
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    const bool act = i < n;
+    const uint32_t k = act ? (uint32_t)s.key[i] : 0xFFFFFFFFu;
+    const uint32_t peers = __match_any_sync(0xffffffffu, k);
+    const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
+    const uint32_t pos = act ? s.off[k] + rank : 0u;
+    __syncwarp();
+    if (act && rank == 0) s.off[k] += __popc(peers);
+    if (act) s.order[pos] = (uint16_t)i;
+    __syncwarp();
+  }
+  // prefix of item counts over the sorted order
+  uint32_t carry = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t it = j < n ? seq_items<BLOCK_M>(load_seq(p, base + s.order[j]), p.Hq) : 0u;
+    const uint32_t incl = warp_incl_scan(it);
+    if (j < n) s.cum[j + 1] = carry + incl;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    s.cum[0] = 0;
+    s.chunk_base = base;
+    s.chunk_n = n;
+  }
+  __syncwarp();
+}
+
+// Work item decoded from the global item index.
+struct WorkItem {
+  int valid;
+  int b, h, qblock;
+  SeqInfo seq;
+};
+
+// One full warp.  Maps global item index w to (sequence, head, query block),
+// loading later chunks as needed (w never decreases within a CTA).
+template <int BLOCK_M>
+__device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
+  WorkItem it;
+  it.valid = 0;
+  while (w >= s.item_end) {
+    const int next = s.chunk_base + s.chunk_n;
+    if (next >= p.B) return it;
+    const unsigned long long base_items = s.item_end;
+    sched_load_chunk<BLOCK_M>(s, p, next);
+    if ((threadIdx.x & 31) == 0) {
+      s.item_base = base_items;
+      s.item_end = base_items + s.cum[s.chunk_n];
+    }
+    __syncwarp();
+  }
+  const uint32_t local = (uint32_t)(w - s.item_base);
+  int lo = 0, hi = s.chunk_n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.cum[mid] <= local) lo = mid; else hi = mid;
+  }
+  it.b = s.chunk_base + s.order[lo];
+  it.seq = load_seq(p, it.b);
+  const uint32_t r = local - s.cum[lo];
+  const uint32_t nblk = (uint32_t)((it.seq.q_len + BLOCK_M - 1) / BLOCK_M);
+  it.h = (int)(r / nblk);
+  it.qblock = (int)(nblk - 1u - (r % nblk));
+  it.valid = 1;
+  return it;
+}
+
+__device__ __forceinline__ void sched_init(SchedSmem& s) {
+  s.chunk_base = 0;
+  s.chunk_n = 0;
+  s.item_base = 0;
+  s.item_end = 0;
+}
+
+// ----------------------------------------------------------------------------
+// Pad rows: every output row outside all [start_b, start_b + len_b) ranges is
+// written as exact zeros (and -inf LSE).  Gap g (0 <= g <= B) is the range
+// between the end of sequence g-1 (0 for g == 0) and the start of sequence g
+// (T for g == B).  Gaps are spread over CTAs; `nthreads` threads starting at
+// thread `t0` of the CTA take part.
+// ----------------------------------------------------------------------------
+__device__ void zero_pad_rows(const AttnParams& p, int t0, int nthreads, int elem_bytes) {
+  const int tid = (int)threadIdx.x - t0;
+  const long long row_bytes = (long long)p.Hq * p.d * elem_bytes;
+  for (int g = blockIdx.x; g <= p.B; g += gridDim.x) {
+    long long a = 0, e = p.T;
+    if (g > 0) {
+      SeqInfo s = load_seq(p, g - 1);
+      a = (long long)s.q_start + s.q_len;
+    }
+    if (g < p.B) {
+      const long long cq = p.cu_q[g];
+      long long st = p.pad_q ? (long long)p.pad_q[g] : cq;
+      e = st < 0 ? 0 : (st > p.T ? p.T : st);
+    }
+    if (e <= a) continue;
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.out) + a * row_bytes);
+    const long long n16 = (e - a) * row_bytes / 16;
+    for (long long i = tid; i < n16; i += nthreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (p.lse) {
+      const long long rows = e - a;
+      for (long long i = tid; i < rows * p.Hq; i += nthreads) {
+        const long long h = i / rows, r = i % rows;
+        p.lse[h * p.T + a + r] = -INFINITY;
+      }
+    }
+  }
+}
+
+template <typename DT>
+struct DTypeTraits;
+template <>
+struct DTypeTraits<__nv_bfloat16> {
+  static constexpr bool kBF16 = true;
+  __device__ static __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ static __forceinline__ float lo(uint32_t x) { return __uint_as_float(x << 16); }
+  __device__ static __forceinline__ float hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+};
+template <>
+struct DTypeTraits<__half> {
+  static constexpr bool kBF16 = false;
+  __device__ static __forceinline__ uint32_t pack2(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ static __forceinline__ float lo(uint32_t x) {
+    return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu)));
+  }
+  __device__ static __forceinline__ float hi(uint32_t x) {
+    return __half2float(__ushort_as_half((unsigned short)(x >> 16)));
+  }
+};
+
+}  // namespace thd

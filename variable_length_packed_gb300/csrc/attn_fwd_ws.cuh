@@ -1,0 +1,447 @@
+// attn_fwd_ws.cuh — the persistent, warp-specialised attention kernel
+// (head_dim 64 or 128, TMA loads).
+//
+// One CTA per SM.  A work item is a block of 256 query rows of one (sequence,
+// head), split into two 128-row Q tiles that share every K/V tile:
+//
+//   warp 0      scheduler + TMA producer: claims items from the global counter,
+//               publishes them to the other warps, loads Q (both tiles) and the
+//               K/V tiles of the item into a two-stage ring.
+//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM (SS UMMA),
+//               then O_i += P_i V_j with P_i read from TMEM (TS UMMA); the two
+//               tiles alternate so one tile's softmax overlaps the other
+//               tile's MMAs.
+//   warps 2-5   softmax of Q tile 0; warps 6-9 softmax of Q tile 1.  One thread
+//               per query row (= TMEM lane): masking, online max / sum, P
+//               (rounded to the input type) written over S in TMEM, lazy O
+//               rescaling (only when the running max grows by more than 2^8),
+//               and the epilogue O / l -> out, LSE.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; P_i
+// occupies the first 64 columns of S_i (two 16-bit values per column).
+#pragma once
+#include "attn_common.cuh"
+
+namespace thd {
+
+constexpr int kWsBlockM = 256;   // query rows per work item (two Q tiles)
+constexpr int kWsStages = 2;     // K/V ring depth
+constexpr int kWsThreads = 320;  // 10 warps
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int DP>
+struct WsSmem {
+  static constexpr int kTileBytes = kTileM * DP * 2;
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t k[kWsStages][kTileBytes];
+  alignas(1024) uint8_t v[kWsStages][kTileBytes];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kWsStages], v_full[kWsStages], kv_empty[kWsStages];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+  WorkItem items[2];
+  SchedSmem sched;
+};
+
+struct ItemGeom {
+  int q0;          // first query position of the block
+  int rows[2];     // valid rows of each Q tile
+  int n[2];        // KV tiles each Q tile visits
+  int n_all;       // KV tiles loaded for the item
+  int kvh;         // key/value head
+};
+
+__device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const AttnParams& p) {
+  ItemGeom g;
+  const SeqInfo& s = it.seq;
+  g.q0 = it.qblock * kWsBlockM;
+  g.rows[0] = min(kTileM, s.q_len - g.q0);
+  g.rows[1] = max(0, min(kTileM, s.q_len - g.q0 - kTileM));
+  g.n[0] = g.rows[0] > 0 ? kv_tiles_for(s, g.q0, kTileM) : 0;
+  g.n[1] = g.rows[1] > 0 ? kv_tiles_for(s, g.q0 + kTileM, kTileM) : 0;
+  g.n_all = max(g.n[0], g.n[1]);
+  g.kvh = it.h / p.group;
+  return g;
+}
+
+template <int DP>
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_smem, uint32_t k_smem, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < DP / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+    umma_ss(tS, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024), idesc,
+            kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_smem, uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2048 bytes) of V
+    umma_ts(tO, tP + kk * 8, smem_desc_sw128(v_smem + kk * 2048, 16384, 1024), idesc,
+            (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Wait that also gives up when the CTA aborted.
+#define WS_WAIT(bar, parity) mbar_wait((bar), (parity), abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs)
+
+// Warp-uniform variant: every lane waits, and the warp gives up together, so the
+// warp-collective tcgen05.ld / tcgen05.st that follow stay convergent.
+#define WS_WAIT_WARP(bar, parity) (__all_sync(0xffffffffu, WS_WAIT((bar), (parity)) ? 1 : 0) != 0)
+
+// Bounded wait used only while draining (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// warp 0: scheduler + TMA producer
+// ---------------------------------------------------------------------------
+template <int DP>
+__device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                            const CUtensorMap* tm_v, volatile uint32_t* abort_flag) {
+  constexpr uint32_t kTileBytes = WsSmem<DP>::kTileBytes;
+  constexpr int kPanels = DP / 64;
+  const int lane = threadIdx.x & 31;
+  uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0;
+  bool ok = true;
+  for (;;) {
+    unsigned long long w = 0;
+    if (lane == 0) w = atomicAdd(p.work_counter, 1ull);
+    w = __shfl_sync(0xffffffffu, w, 0);
+    WorkItem it = sched_decode<kWsBlockM>(sm.sched, p, w);
+    const int slot = it_cnt & 1;
+    if (lane == 0) {
+      if (it_cnt >= 2) ok = WS_WAIT(&sm.item_empty[slot], ((it_cnt >> 1) - 1) & 1);
+      if (!ok) it.valid = 0;
+      sm.items[slot] = it;
+      mbar_arrive(&sm.item_full[slot]);
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    ++it_cnt;
+    if (!it.valid || !ok) break;
+    const ItemGeom g = item_geom(it, p);
+    if (g.n_all == 0) continue;
+    if (lane == 0) {
+      const SeqInfo& s = it.seq;
+      if (q_cnt >= 1) ok = WS_WAIT(&sm.q_empty, (q_cnt - 1) & 1);
+      if (ok) {
+        const int ntiles = g.rows[1] > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(&sm.q_full, ntiles * kTileBytes);
+        for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+          for (int pn = 0; pn < kPanels; ++pn)
+            tma_load_2d(sm.q[t] + pn * 16384, tm_q, &sm.q_full, it.h * p.d + pn * 64, s.q_start + g.q0 + t * kTileM);
+        ++q_cnt;
+      }
+      for (int j = 0; ok && j < g.n_all; ++j) {
+        const int st = kv_cnt % kWsStages;
+        if (kv_cnt >= kWsStages) ok = WS_WAIT(&sm.kv_empty[st], ((kv_cnt / kWsStages) - 1) & 1);
+        if (!ok) break;
+        const int row = s.kv_start + j * kBlockN;
+        mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+#pragma unroll
+        for (int pn = 0; pn < kPanels; ++pn)
+          tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], g.kvh * p.d + pn * 64, row);
+        mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+#pragma unroll
+        for (int pn = 0; pn < kPanels; ++pn)
+          tma_load_2d(sm.v[st] + pn * 16384, tm_v, &sm.v_full[st], g.kvh * p.d + pn * 64, row);
+        ++kv_cnt;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+  }
+  // copies still in flight land before the CTA can exit
+  if (lane == 0) {
+    if (q_cnt > 0) drain_wait(&sm.q_full, (q_cnt - 1) & 1);
+    for (uint32_t c = (kv_cnt > kWsStages ? kv_cnt - kWsStages : 0); c < kv_cnt; ++c) {
+      drain_wait(&sm.k_full[c % kWsStages], (c / kWsStages) & 1);
+      drain_wait(&sm.v_full[c % kWsStages], (c / kWsStages) & 1);
+    }
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// warp 1 (one thread): MMA issuer
+// ---------------------------------------------------------------------------
+template <typename DT, int DP>
+__device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volatile uint32_t* abort_flag) {
+  using Tr = DTypeTraits<DT>;
+  constexpr uint32_t idesc_qk = umma_idesc_f16(Tr::kBF16, kTileM, kBlockN, false);
+  constexpr uint32_t idesc_pv = umma_idesc_f16(Tr::kBF16, kTileM, DP, true);
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO[2] = {tmem + 256, tmem + 256 + DP};
+  uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, p_cnt[2] = {0, 0};
+  for (;;) {
+    const int slot = it_cnt & 1;
+    if (!WS_WAIT(&sm.item_full[slot], (it_cnt >> 1) & 1)) break;
+    const WorkItem it = sm.items[slot];
+    mbar_arrive(&sm.item_empty[slot]);
+    ++it_cnt;
+    if (!it.valid) break;
+    const ItemGeom g = item_geom(it, p);
+    const int n = g.n_all;
+    if (n == 0) continue;
+    if (!WS_WAIT(&sm.q_full, q_cnt & 1)) break;
+    ++q_cnt;
+    if (!WS_WAIT(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
+    tc_fence_after();
+    {
+      const uint32_t ks = smem_u32(sm.k[kv_cnt % kWsStages]);
+      for (int t = 0; t < 2; ++t) {
+        if (g.n[t] > 0) {
+          issue_qk<DP>(tS[t], smem_u32(sm.q[t]), ks, idesc_qk);
+          umma_commit(&sm.s_full[t]);
+        }
+      }
+      if (n == 1) umma_commit(&sm.q_empty);
+    }
+    bool ok = true;
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t c = kv_cnt + j, cn = c + 1;
+      const int st = c % kWsStages, stn = cn % kWsStages;
+      if (!WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
+      const uint32_t vs = smem_u32(sm.v[st]);
+      for (int t = 0; t < 2; ++t) {
+        if (j >= g.n[t]) continue;
+        if (!WS_WAIT(&sm.p_full[t], p_cnt[t] & 1)) { ok = false; break; }
+        ++p_cnt[t];
+        tc_fence_after();
+        issue_pv(tO[t], tS[t], vs, idesc_pv, j > 0);
+        umma_commit(&sm.o_full[t]);
+        if (j + 1 < g.n[t]) {
+          if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk<DP>(tS[t], smem_u32(sm.q[t]), smem_u32(sm.k[stn]), idesc_qk);
+          umma_commit(&sm.s_full[t]);
+        }
+      }
+      if (j == n - 2) umma_commit(&sm.q_empty);   // last S MMAs of the item issued
+      umma_commit(&sm.kv_empty[st]);
+    }
+    kv_cnt += n;
+    if (!ok) break;
+  }
+  // every MMA issued so far completes before TMEM is released
+  umma_commit(&sm.drain);
+  drain_wait(&sm.drain, 0);
+}
+
+// ---------------------------------------------------------------------------
+// warps 2-9: softmax + epilogue, tile = (warp - 2) / 4
+// ---------------------------------------------------------------------------
+template <typename DT, int DP>
+__device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, int tile,
+                           volatile uint32_t* abort_flag) {
+  using Tr = DTypeTraits<DT>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row = 32 * (warp & 3) + lane;           // TMEM lane = row of the Q tile
+  const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tS = tmem + 128 * tile + t_lane;
+  const uint32_t tO = tmem + 256 + DP * tile + t_lane;
+  const float sl2 = p.scale_log2;
+  uint32_t it_cnt = 0, s_cnt = 0, o_cnt = 0;
+
+  for (;;) {
+    const int slot = it_cnt & 1;
+    if (!WS_WAIT_WARP(&sm.item_full[slot], (it_cnt >> 1) & 1)) break;
+    const WorkItem it = sm.items[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
+    ++it_cnt;
+    if (!it.valid) break;
+    const ItemGeom g = item_geom(it, p);
+    const SeqInfo& s = it.seq;
+    const int ni = g.n[tile];
+    const int rows = g.rows[tile];
+    const int qt0 = g.q0 + kTileM * tile;             // first query position of this tile
+    const int qpos = qt0 + row;
+
+    float m_run = -INFINITY;
+    float lr[4] = {0.f, 0.f, 0.f, 0.f};   // rounded-P sums (normalise O)
+    float le[4] = {0.f, 0.f, 0.f, 0.f};   // exact sums (LSE)
+    bool ok = true;
+    for (int j = 0; j < ni; ++j) {
+      if (!WS_WAIT_WARP(&sm.s_full[tile], s_cnt & 1)) { ok = false; break; }
+      ++s_cnt;
+      tc_fence_after();
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
+      tmem_ld_wait_regs32(sr);
+      tmem_tie_regs32(sr + 32);
+      tmem_tie_regs32(sr + 64);
+      tmem_tie_regs32(sr + 96);
+
+      const int kv0 = j * kBlockN;
+      if (kv0 + kBlockN > s.kv_len || (s.causal && kv0 + kBlockN - 1 > qt0)) {
+        const int lim = s.causal ? min(s.kv_len - 1, qpos) - kv0 : s.kv_len - 1 - kv0;   // last visible column
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(sr[c + u]));
+      }
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float m_new = fmaxf(m_run, m_tile);
+      const bool need = (m_new - m_run) * sl2 > kRescaleThreshold;   // false while both are -inf
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx((m_run - m_new) * sl2);
+        m_run = m_new;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          lr[u] *= alpha;
+          le[u] *= alpha;
+        }
+      }
+      const float mb = (m_run == -INFINITY ? 0.f : m_run) * sl2;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x0 = ex2_approx(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -mb));
+          const float x1 = ex2_approx(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -mb));
+          pk[e] = Tr::pack2(x0, x1);
+          le[e & 3] += x0 + x1;
+          lr[e & 3] += Tr::lo(pk[e]) + Tr::hi(pk[e]);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O_i must hold the previous P V product before it is rescaled
+        if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DP / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait_regs32(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[tile]);
+    }
+    if (!ok) break;
+    o_cnt += ni;
+
+    // ---- epilogue ----
+    const bool row_ok = row < rows;
+    DT* dst = static_cast<DT*>(p.out) + ((size_t)(s.q_start + (row_ok ? qpos : 0)) * p.Hq + it.h) * (size_t)p.d;
+    if (ni > 0) {
+      if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt - 1) & 1)) break;
+      tc_fence_after();
+      const float l_r = (lr[0] + lr[1]) + (lr[2] + lr[3]);
+      const float l_e = (le[0] + le[1]) + (le[2] + le[3]);
+      const float inv = 1.f / l_r;
+#pragma unroll
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_ld_wait_regs32(o);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v4;
+            v4.x = Tr::pack2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v4.y = Tr::pack2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v4.z = Tr::pack2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v4.w = Tr::pack2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + 32 * c + e) = v4;
+          }
+        }
+      }
+      if (row_ok && p.lse) p.lse[(size_t)it.h * p.T + s.q_start + qpos] = m_run * p.scale + logf(l_e);
+    } else if (row_ok) {
+#pragma unroll
+      for (int col = 0; col < DP; col += 8) *reinterpret_cast<uint4*>(dst + col) = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse) p.lse[(size_t)it.h * p.T + s.q_start + qpos] = -INFINITY;
+    }
+    tc_fence_before();
+  }
+}
+
+template <typename DT, int DP>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  WsSmem<DP>& sm = *reinterpret_cast<WsSmem<DP>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < kWsStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_full[t], 1);
+      mbar_init(&sm.item_full[t], 1);
+      mbar_init(&sm.item_empty[t], 9);   // MMA thread + one lane of each softmax warp
+    }
+    mbar_init(&sm.drain, 1);
+    fence_mbar_init();
+    sm.abort = 0;
+    sched_init(sm.sched);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile uint32_t* abort_flag = &sm.abort;
+
+  if (warp == 0) {
+    ws_producer<DP>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) ws_mma<DT, DP>(sm, p, tmem, abort_flag);
+    __syncwarp();
+  } else {
+    zero_pad_rows(p, 64, kWsThreads - 64, 2);
+    ws_softmax<DT, DP>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+#undef WS_WAIT
+#undef WS_WAIT_WARP
+
+}  // namespace thd

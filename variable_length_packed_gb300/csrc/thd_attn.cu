@@ -1,0 +1,203 @@
+// thd_attn.cu — the C ABI of libthdattn.so (declared in include/thd_attn.h):
+// host-side argument validation, TMA tensor-map encoding and kernel launches.
+// Nothing here reads device memory or synchronises a stream.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/thd_attn.h"
+#include "attn_fwd_serial.cuh"
+#include "attn_fwd_ws.cuh"
+
+namespace thd {
+cudaError_t launch_padding_mask(const int32_t* cu, int B, int S, uint8_t* mask, int num_sms, cudaStream_t stream);
+}
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = 256;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int num_sms_of_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2-D view [rows, heads * d] of a THD tensor, box = 128 rows x 64 columns,
+// 128-byte swizzle (the layout the UMMA shared-memory descriptors expect).
+bool encode_thd_map(CUtensorMap* map, const void* base, int rows, int heads, int d, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)heads * (cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)heads * (cuuint64_t)d * 2ull};
+  cuuint32_t box[2] = {64u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename DT, int DP, bool kTMA>
+int launch_serial(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const thd::AttnParams& p,
+                  int grid, cudaStream_t stream) {
+  auto kern = thd::attn_fwd_serial_kernel<DT, DP, kTMA>;
+  const size_t smem = sizeof(thd::SerialSmem<DP>) + 1024;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return THD_ERR_CUDA;
+  kern<<<grid, 128, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
+}
+
+template <typename DT, int DP>
+int launch_ws(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const thd::AttnParams& p,
+              int grid, cudaStream_t stream) {
+  auto kern = thd::attn_fwd_ws_kernel<DT, DP>;
+  const size_t smem = sizeof(thd::WsSmem<DP>) + 1024;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return THD_ERR_CUDA;
+  kern<<<grid, thd::kWsThreads, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* thd_status_string(int status) {
+  switch (status) {
+    case THD_OK: return "THD_OK";
+    case THD_ERR_ARG: return "THD_ERR_ARG: invalid argument";
+    case THD_ERR_UNSUPPORTED: return "THD_ERR_UNSUPPORTED: unsupported head_dim, dtype or head layout";
+    case THD_ERR_CUDA: return "THD_ERR_CUDA: CUDA call failed";
+    case THD_ERR_WORKSPACE: return "THD_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    default: return "unknown thd_status";
+  }
+}
+
+size_t thd_attn_workspace_size(void) { return kWorkspaceBytes; }
+
+int thd_padding_mask(const int32_t* cu_seqlens, int batch_size, int max_seqlen, uint8_t* mask, void* stream) {
+  if (batch_size < 0 || max_seqlen < 0) return THD_ERR_ARG;
+  if (batch_size == 0 || max_seqlen == 0) return THD_OK;
+  if (!cu_seqlens || !mask) return THD_ERR_ARG;
+  if (!aligned(cu_seqlens, 4)) return THD_ERR_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return THD_ERR_CUDA;
+  cudaError_t e = thd::launch_padding_mask(cu_seqlens, batch_size, max_seqlen, mask, sms,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? THD_OK : THD_ERR_CUDA;
+}
+
+int thd_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size,
+                 int max_seqlen, float softmax_scale, void* out, float* lse, int total_tokens, int num_heads_q,
+                 int num_heads_kv, int head_dim, int dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  // ---- host-checkable arguments ----
+  if (batch_size < 0 || max_seqlen < 0 || total_tokens < 0) return THD_ERR_ARG;
+  if (num_heads_q < 1 || num_heads_kv < 1) return THD_ERR_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return THD_ERR_ARG;
+  if (dtype != THD_BF16 && dtype != THD_FP16) return THD_ERR_UNSUPPORTED;
+  if (head_dim < 8 || head_dim > 128 || head_dim % 8 != 0) return THD_ERR_UNSUPPORTED;
+  if (num_heads_q % num_heads_kv != 0) return THD_ERR_UNSUPPORTED;
+  // scheduler counters are 32-bit per chunk of sequences
+  const long long max_items = ((long long)total_tokens / 128 + (long long)batch_size + 1) * num_heads_q;
+  if (max_items >= (1ll << 31)) return THD_ERR_UNSUPPORTED;
+  if ((long long)num_heads_q * head_dim * 2 >= (1ll << 31)) return THD_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return THD_OK;   // no rows: nothing to write
+  if (!q || !k || !v || !out) return THD_ERR_ARG;
+  if (batch_size > 0 && (!cu_seqlens_q || !cu_seqlens_kv)) return THD_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return THD_ERR_ARG;
+  if ((lse && !aligned(lse, 4)) || (cu_seqlens_q && !aligned(cu_seqlens_q, 4)) ||
+      (cu_seqlens_kv && !aligned(cu_seqlens_kv, 4)) ||
+      (cu_seqlens_q_padded && !aligned(cu_seqlens_q_padded, 4)) ||
+      (cu_seqlens_kv_padded && !aligned(cu_seqlens_kv_padded, 4)))
+    return THD_ERR_ARG;
+  if (!workspace || !aligned(workspace, 16) || workspace_bytes < kWorkspaceBytes) return THD_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return THD_ERR_CUDA;
+
+  thd::AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.pad_q = cu_seqlens_q_padded;
+  p.pad_kv = cu_seqlens_kv_padded;
+  p.causal = seq_is_causal;
+  p.out = out;
+  p.lse = lse;
+  p.work_counter = static_cast<unsigned long long*>(workspace);
+  p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
+  p.B = batch_size;
+  p.T = total_tokens;
+  p.Hq = num_heads_q;
+  p.Hkv = num_heads_kv;
+  p.d = head_dim;
+  p.group = num_heads_q / num_heads_kv;
+  p.scale = softmax_scale;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  // work counter and status word start at zero for this call
+  if (cudaMemsetAsync(workspace, 0, 16, st) != cudaSuccess) return THD_ERR_CUDA;
+
+  const bool bf16 = dtype == THD_BF16;
+  const bool tma = head_dim == 64 || head_dim == 128;
+  CUtensorMap mq, mk, mv;
+  std::memset(&mq, 0, sizeof(mq));
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  if (tma) {
+    if (!encode_thd_map(&mq, q, total_tokens, num_heads_q, head_dim, bf16) ||
+        !encode_thd_map(&mk, k, total_tokens, num_heads_kv, head_dim, bf16) ||
+        !encode_thd_map(&mv, v, total_tokens, num_heads_kv, head_dim, bf16))
+      return THD_ERR_CUDA;
+  }
+  const int grid = sms;
+  if (bf16) {
+    if (head_dim == 128) return launch_ws<__nv_bfloat16, 128>(mq, mk, mv, p, grid, st);
+    if (head_dim == 64) return launch_ws<__nv_bfloat16, 64>(mq, mk, mv, p, grid, st);
+    if (head_dim < 64) return launch_serial<__nv_bfloat16, 64, false>(mq, mk, mv, p, grid, st);
+    return launch_serial<__nv_bfloat16, 128, false>(mq, mk, mv, p, grid, st);
+  } else {
+    if (head_dim == 128) return launch_ws<__half, 128>(mq, mk, mv, p, grid, st);
+    if (head_dim == 64) return launch_ws<__half, 64>(mq, mk, mv, p, grid, st);
+    if (head_dim < 64) return launch_serial<__half, 64, false>(mq, mk, mv, p, grid, st);
+    return launch_serial<__half, 128, false>(mq, mk, mv, p, grid, st);
+  }
+}
+
+}  // extern "C"
