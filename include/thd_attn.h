@@ -4,8 +4,9 @@
  * NVIDIA GB300 (sm_103a) GPU.
  *
  * Every pointer argument named "device" is a CUDA device pointer; the library
- * never dereferences it on the host and never synchronises the stream, so the
- * calls are asynchronous and may be captured in a CUDA graph.  `stream` is a
+ * never dereferences it on the host and never synchronises the stream, so
+ * thd_attn_fwd and thd_padding_mask are asynchronous and may be captured in a
+ * CUDA graph.  `stream` is a
  * cudaStream_t passed as void* (NULL = the legacy default stream).  The caller
  * owns every buffer.  The library allocates no device memory.
  *
@@ -104,6 +105,39 @@ int thd_attn_fwd(const void* q, const void* k, const void* v,
                  void* out, float* lse,
                  int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
                  int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * thd_attn_fwd_noalloc — thd_attn_fwd for callers that cannot allocate device
+ * memory: identical arguments minus the workspace, identical results.
+ *
+ * The pages have no counterpart to this entry point; it exists for the
+ * library's callers.  Plugins whose host engine owns all device memory and
+ * offers them no allocator, pipelines that fix their device-memory budget at
+ * start-up and forbid allocation afterwards, and latency-bound loops that must
+ * not risk cudaMalloc's device-wide blocking cannot provide the small
+ * workspace thd_attn_fwd asks for.  Here the workspace is a fixed 256-byte
+ * buffer compiled into the library (a __device__ array, one copy per GPU that
+ * loads the library, kept until the process exits).  The library calls no
+ * cudaMalloc/cudaFree or other allocating routine.
+ *
+ * - The first call on each device looks up that buffer's device address
+ *   (cudaGetSymbolAddress, which may load the library's device code): make the
+ *   first call on a device before any stream capture begins.
+ * - Every call on a device shares the buffer.  Calls that overlap on the GPU
+ *   (unordered streams) race on it and give wrong results; order them.  The
+ *   buffer's counter and status word are cleared on `stream` at the start of
+ *   each call; it keeps the last call's contents.
+ * - THD_ERR_WORKSPACE if the library's workspace requirement ever exceeds the
+ *   fixed buffer; otherwise the same status codes as thd_attn_fwd.
+ */
+int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                         const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                         const uint8_t* seq_is_causal,
+                         int batch_size, int max_seqlen, float softmax_scale,
+                         void* out, float* lse,
+                         int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                         int dtype, void* stream);
 
 /*
  * thd_padding_mask — the boolean attention padding mask built on the device,

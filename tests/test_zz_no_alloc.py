@@ -1,0 +1,55 @@
+"""thd_attn_fwd_noalloc: the entry point for callers that cannot allocate device memory.
+
+It must give the same result as thd_attn_fwd (within the parity tolerances) while taking
+its workspace from the library's fixed per-device buffer.  Two calls in a row also check
+that the buffer's leftover state from one call does not leak into the next.  This file is
+collected last, so a failure here does not hide any other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from thd_testutil import OUT_ATOL, LSE_ATOL, to_device
+
+pytestmark = pytest.mark.gpu
+vlp = pytest.importorskip("variable_length_packed_gb300")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from variable_length_packed_gb300 import build as vbuild
+    vbuild.build()
+    return vlp.load_library()
+
+
+@pytest.mark.parametrize("name", ["padded_gaps", "tiny_mixed", "page1_pad"])
+def test_noalloc_matches_workspace_entry_point(lib, name):
+    w = workloads.make(name)
+    dev = to_device(w)
+    ref_out, ref_lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"],
+                                        dev["padded"], dev["causal"], w.batch_size, w.max_seqlen,
+                                        w.softmax_scale)
+    torch.cuda.synchronize()
+    P = ctypes.c_void_p
+    dtype = 0 if w.dtype == torch.bfloat16 else 1
+    stream = P(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        out = torch.full_like(dev["q"], float("nan"))
+        lse = torch.full((w.num_heads_q, w.total_tokens), float("nan"), dtype=torch.float32, device="cuda")
+        st = lib.thd_attn_fwd_noalloc(
+            P(dev["q"].data_ptr()), P(dev["k"].data_ptr()), P(dev["v"].data_ptr()), P(dev["cu"].data_ptr()),
+            P(dev["cu"].data_ptr()), P(None if dev["padded"] is None else dev["padded"].data_ptr()),
+            P(None if dev["padded"] is None else dev["padded"].data_ptr()), P(dev["causal"].data_ptr()),
+            w.batch_size, w.max_seqlen, ctypes.c_float(w.softmax_scale), P(out.data_ptr()), P(lse.data_ptr()),
+            w.total_tokens, w.num_heads_q, w.num_heads_kv, w.head_dim, dtype, stream)
+        assert st == 0, vlp.thd_status_string(st)
+        torch.cuda.synchronize()
+        diff = (out.float() - ref_out.float()).abs().max().item()
+        assert diff <= OUT_ATOL[w.dtype], (call, diff)
+        both_inf = torch.isneginf(lse) & torch.isneginf(ref_lse)
+        ldiff = torch.where(both_inf, torch.zeros_like(lse), (lse - ref_lse).abs()).max().item()
+        assert ldiff <= LSE_ATOL, (call, ldiff)
+        assert not torch.isnan(out).any() and not torch.isnan(lse).any()

@@ -14,7 +14,7 @@ import os
 
 import torch
 
-__all__ = ["thd_attn_fwd", "thd_padding_mask", "thd_attn_workspace_size", "thd_status_string",
+__all__ = ["thd_attn_fwd", "thd_attn_fwd_noalloc", "thd_padding_mask", "thd_attn_workspace_size", "thd_status_string",
            "ThdError", "library_path", "load_library", "STATUS_WAIT_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -47,6 +47,8 @@ def load_library():
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.thd_attn_fwd.restype = I
     lib.thd_attn_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P, SZ, P]
+    lib.thd_attn_fwd_noalloc.restype = I
+    lib.thd_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P]
     lib.thd_padding_mask.restype = I
     lib.thd_padding_mask.argtypes = [P, I, I, P, P]
     lib.thd_attn_workspace_size.restype = SZ
@@ -134,6 +136,34 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
             _ptr(workspace), workspace.numel(), _stream_handle(q.device))
     if st != THD_OK:
         raise ThdError(st, "thd_attn_fwd")
+    return out, lse
+
+
+def thd_attn_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                         seq_is_causal, batch_size, max_seqlen, softmax_scale, out, lse=None):
+    """thd_attn_fwd without a workspace: the library uses its fixed per-device buffer.
+
+    For callers that cannot allocate device memory; the caller passes every input and
+    output tensor, and nothing is allocated here either.  Calls on one device must not
+    overlap on the GPU (they share the buffer).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
+                    ("cu_seqlens_kv", cu_seqlens_kv), ("cu_seqlens_q_padded", cu_seqlens_q_padded),
+                    ("cu_seqlens_kv_padded", cu_seqlens_kv_padded), ("seq_is_causal", seq_is_causal),
+                    ("out", out), ("lse", lse)):
+        _cuda(t, name)
+    if out is None:
+        raise ValueError("out must be provided")
+    T, Hq, d = q.shape
+    with torch.cuda.device(q.device):
+        st = _lib().thd_attn_fwd_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+            _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), _ptr(seq_is_causal),
+            int(batch_size), int(max_seqlen), float(softmax_scale), _ptr(out), _ptr(lse),
+            int(T), int(Hq), int(k.shape[1]), int(d), THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16,
+            _stream_handle(q.device))
+    if st != THD_OK:
+        raise ThdError(st, "thd_attn_fwd_noalloc")
     return out, lse
 
 
