@@ -213,7 +213,7 @@ def oracle_sample(w, budget_s):
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
-    w = workloads.make(WORKLOAD)
+    w = workloads.make(args.workload)
     eff = effective_flops(w)
     per_step = []
     descs = []
@@ -265,7 +265,7 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    w = workloads.make(WORKLOAD)
+    w = workloads.make(args.workload)
     eff = effective_flops(w)
     stream = torch.cuda.current_stream(dev)
 
@@ -307,6 +307,11 @@ def run_gpu(args, ws, rank, local):
     elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / args.steps
     value = ws * eff / (ms_per_step * 1e-3) / 1e12
+    if args.attn_only:
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "attn_ms_per_launch": attn_ms,
+                              "effective_tflops": eff / (attn_ms * 1e-3) / 1e12, "status": status}), flush=True)
+        return 0
 
     # ---- padding mask alone on the 4096 x 8192 workload (CUDA graph of back-to-back launches) ----
     mw = workloads.make_mask()
@@ -418,6 +423,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS),
+                    help="packed batch to run (default: the long-context workload the metric is quoted on)")
+    ap.add_argument("--attn-only", action="store_true",
+                    help="run only the attention launches (warm-up + timed) and print the line; "
+                         "for profiler captures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
     ws, rank, local = dist_setup()

@@ -6,101 +6,138 @@
 // 0..B of cu are read (Changes: longer buffers are allowed), and a sequence
 // longer than S gives an all-False row (Equivalence).
 //
-// The output is a pure HBM write stream: each thread writes whole 16-byte
-// chunks of the flat B*S byte array (coalesced 512-byte warp stores), walking
-// the row index forward inside the chunk; the unaligned head and tail bytes
-// of the buffer are written one byte at a time.
+// The output is a pure HBM write stream.  Each thread writes whole 16-byte
+// chunks of the flat B*S byte array (a warp store covers 512 contiguous
+// bytes).  Within one row the mask bytes of a chunk form a step (0 ... 0 1 ... 1),
+// so a chunk is built from at most two steps with 64-bit shifts instead of 16
+// compares.  The chunk's row is found with one exact division by the invariant
+// S: a multiply-high by a reciprocal precomputed on the host (division by
+// invariant integers using multiplication, Granlund & Montgomery, 1994).  The
+// unaligned head and tail bytes of the buffer are written one at a time.
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace thd {
 
-__device__ __forceinline__ int row_len(const int32_t* cu, long long b) {
-  return (int)((long long)cu[b + 1] - (long long)cu[b]);
+namespace {
+
+constexpr uint64_t kOnes = 0x0101010101010101ull;
+
+struct MaskArgs {
+  const int32_t* cu;
+  uint8_t* mask;
+  long long S;
+  long long total;     // B * S
+  long long head;      // bytes before the first 16-byte aligned address
+  long long nchunks;   // aligned 16-byte chunks
+  uint64_t recip;      // floor((2^64 - 1) / S) + 1, exact quotient for numerators < 2^32
+  int div32;           // total < 2^32: use the reciprocal
+};
+
+__device__ __forceinline__ long long row_len(const int32_t* cu, long long b) {
+  return (long long)cu[b + 1] - (long long)cu[b];
 }
 
-// Mask bytes [f, f + n) of the flat array, n <= 16, packed little-endian.
-__device__ __forceinline__ void mask_bytes(const int32_t* cu, long long S, long long f, int n, uint8_t* out) {
-  long long b = f / S;
-  long long p = f - b * S;
-  long long len = row_len(cu, b);
-  for (int i = 0; i < n; ++i) {
-    out[i] = (uint8_t)(p >= len ? 1 : 0);
-    if (++p == S) {
-      p = 0;
-      ++b;
-      if (i + 1 < n) len = row_len(cu, b);
-    }
+__device__ __forceinline__ void div_row(const MaskArgs& a, long long f, long long& b, long long& p) {
+  if (a.div32) {
+    b = (a.S == 1) ? f : (long long)__umul64hi((unsigned long long)f, a.recip);
+  } else {
+    b = f / a.S;
   }
+  p = f - b * a.S;
 }
 
-__global__ void __launch_bounds__(256) padding_mask_kernel(const int32_t* __restrict__ cu, long long S,
-                                                            uint8_t* __restrict__ mask, long long total,
-                                                            long long head, long long nchunks) {
+// 16 mask bytes (two little-endian words) with bytes [t, 16) set, t in [0, 16].
+__device__ __forceinline__ void step_from(int t, uint64_t& lo, uint64_t& hi) {
+  lo = t >= 8 ? 0ull : (kOnes << (8 * t));
+  hi = t >= 16 ? 0ull : (t <= 8 ? kOnes : (kOnes << (8 * (t - 8))));
+}
+
+__device__ __forceinline__ int clampi(long long x, int lo, int hi) {
+  return (int)(x < lo ? lo : (x > hi ? hi : x));
+}
+
+__device__ __forceinline__ uint8_t mask_byte(const MaskArgs& a, long long f) {
+  long long b, p;
+  div_row(a, f, b, p);
+  return (uint8_t)(p >= row_len(a.cu, b) ? 1 : 0);
+}
+
+// Chunk starting at flat byte f (S >= 16: the chunk spans at most two rows).
+__device__ __forceinline__ uint4 mask_chunk(const MaskArgs& a, long long f) {
+  long long b, p0;
+  div_row(a, f, b, p0);
+  const long long len0 = row_len(a.cu, b);
+  const int e0 = (int)(a.S - p0 < 16 ? a.S - p0 : 16);   // bytes of row b in the chunk
+  const int t0 = clampi(len0 - p0, 0, e0);                // first padded byte of row b
+  uint64_t lo, hi, lo_e, hi_e;
+  step_from(t0, lo, hi);
+  step_from(e0, lo_e, hi_e);
+  lo &= ~lo_e;
+  hi &= ~hi_e;
+  if (e0 < 16) {                                          // row b + 1 fills the rest
+    const long long len1 = row_len(a.cu, b + 1);
+    const int t1 = e0 + clampi(len1, 0, 16 - e0);
+    uint64_t lo1, hi1;
+    step_from(t1, lo1, hi1);
+    lo |= lo1;
+    hi |= hi1;
+  }
+  return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+}
+
+__global__ void __launch_bounds__(256) padding_mask_kernel(const MaskArgs a) {
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  // unaligned head and tail bytes
-  if (tid < head) {
-    uint8_t v;
-    mask_bytes(cu, S, tid, 1, &v);
-    mask[tid] = v;
-  }
-  const long long tail0 = head + nchunks * 16;
-  if (tid < total - tail0) {
-    uint8_t v;
-    mask_bytes(cu, S, tail0 + tid, 1, &v);
-    mask[tail0 + tid] = v;
-  }
-  uint4* body = reinterpret_cast<uint4*>(mask + head);
-  if (S >= 16) {
-    // a 16-byte chunk spans at most two rows: one division per chunk
-    for (long long c = tid; c < nchunks; c += stride) {
-      const long long f = head + c * 16;
-      const long long b = f / S;
-      const long long p0 = f - b * S;
-      const long long len0 = row_len(cu, b);
-      const long long split = S - p0;   // bytes left in row b
-      const long long len1 = split < 16 ? (long long)row_len(cu, b + 1) : 0;
+  if (tid < a.head) a.mask[tid] = mask_byte(a, tid);
+  const long long tail0 = a.head + a.nchunks * 16;
+  if (tid < a.total - tail0) a.mask[tail0 + tid] = mask_byte(a, tail0 + tid);
+  uint4* body = reinterpret_cast<uint4*>(a.mask + a.head);
+  if (a.S >= 16) {
+    long long c = tid;
+    for (; c + stride < a.nchunks; c += 2 * stride) {     // two independent chunks in flight
+      const uint4 v0 = mask_chunk(a, a.head + c * 16);
+      const uint4 v1 = mask_chunk(a, a.head + (c + stride) * 16);
+      body[c] = v0;
+      body[c + stride] = v1;
+    }
+    if (c < a.nchunks) body[c] = mask_chunk(a, a.head + c * 16);
+  } else {
+    for (long long c = tid; c < a.nchunks; c += stride) {
       uint32_t w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int k = q * 4 + i;
-          const bool pad = (k < split) ? (p0 + k >= len0) : ((long long)k - split >= len1);
-          word |= (pad ? 1u : 0u) << (8 * i);
-        }
+        for (int i = 0; i < 4; ++i) word |= (uint32_t)mask_byte(a, a.head + c * 16 + 4 * q + i) << (8 * i);
         w[q] = word;
       }
-      body[c] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  } else {
-    for (long long c = tid; c < nchunks; c += stride) {
-      uint8_t bytes[16];
-      mask_bytes(cu, S, head + c * 16, 16, bytes);
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        w[q] = bytes[4 * q] | (bytes[4 * q + 1] << 8) | (bytes[4 * q + 2] << 16) | ((uint32_t)bytes[4 * q + 3] << 24);
       body[c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
 
+}  // namespace
+
 // Host launcher (called from the C ABI in thd_attn.cu after validation).
 cudaError_t launch_padding_mask(const int32_t* cu, int B, int S, uint8_t* mask, int num_sms, cudaStream_t stream) {
-  const long long total = (long long)B * (long long)S;
+  MaskArgs a;
+  a.cu = cu;
+  a.mask = mask;
+  a.S = S;
+  a.total = (long long)B * (long long)S;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(mask);
-  long long head = (long long)((16 - (addr & 15)) & 15);
-  if (head > total) head = total;
-  const long long nchunks = (total - head) / 16;
+  a.head = (long long)((16 - (addr & 15)) & 15);
+  if (a.head > a.total) a.head = a.total;
+  a.nchunks = (a.total - a.head) / 16;
+  a.div32 = a.total <= 0xFFFFFFFFll ? 1 : 0;
+  a.recip = S > 1 ? (0xFFFFFFFFFFFFFFFFull / (uint64_t)S) + 1ull : 0ull;
   const int threads = 256;
-  long long want = (nchunks + threads - 1) / threads;
+  long long want = (a.nchunks + 2 * threads - 1) / (2 * threads);
   if (want < 1) want = 1;
   const long long cap = (long long)num_sms * 8;   // 8 resident 256-thread blocks per SM
   const int grid = (int)(want < cap ? want : cap);
-  padding_mask_kernel<<<grid, threads, 0, stream>>>(cu, (long long)S, mask, total, head, nchunks);
+  padding_mask_kernel<<<grid, threads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

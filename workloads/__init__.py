@@ -237,6 +237,16 @@ def long_context(seed=3):
                         with_padded=False)
 
 
+def long_context_small(seed=3):
+    """The long-context mix at a quarter of the size (4 sequences, 32768 tokens, 3 causal /
+    1 full, 16 heads, d=128, bf16): Q/K/V still larger than L2, one launch about a millisecond.
+    Used for profiler captures of the same kernel."""
+    lengths = long_context_lengths(np.random.default_rng(seed), 4, total=32768)
+    causal = np.array([True, True, False, True])
+    return from_lengths("long_context_small", lengths, causal, heads_q=16, head_dim=128,
+                        dtype=torch.bfloat16, seed=seed, with_padded=False)
+
+
 def many_short(seed=4):
     """4096 sequences, lengths geometric (mean 64) clipped to [1, 256], causal ~ Bernoulli(0.3),
     gaps U{0..15} between sequences, 32 heads, d=64, fp16."""
@@ -257,6 +267,7 @@ WORKLOADS = {
     "padded_gaps": padded_gaps,
     "mixed_gqa": mixed_gqa,
     "long_context": long_context,
+    "long_context_small": long_context_small,
     "many_short": many_short,
 }
 
