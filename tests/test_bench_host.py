@@ -1,0 +1,75 @@
+"""Host-side checks of bench.py: the effective-FLOP count, the multi-rank timing path
+(two gloo ranks on CPU) and the reference (oracle) arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch
+
+import bench
+import workloads
+from conftest import ROOT
+
+
+def test_effective_flops_counts_unmasked_pairs():
+    w = workloads.from_lengths("f", [1, 5, 3, 8], [1, 0, 1, 1], heads_q=3, head_dim=16, seed=0)
+    pairs = 0
+    for L, c in zip(w.lengths, w.causal):
+        pairs += sum(1 for i in range(L) for j in range(L) if (j <= i or not c))
+    assert bench.effective_flops(w) == 4 * 16 * 3 * pairs
+
+
+def test_attn_bytes_formula():
+    w = workloads.from_lengths("b", [4, 6], [1, 0], heads_q=4, heads_kv=2, head_dim=8, seed=0)
+    T = w.total_tokens
+    assert bench.attn_bytes(w) == T * 4 * 8 * 2 * 2 + T * 2 * 8 * 2 * 2 + T * 4 * 4
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench as b
+    ws, r, _ = b.dist_setup()
+    assert dist.get_backend() == "gloo"
+    b.barrier(ws)
+    t = b.max_over_ranks(1.5 * (r + 1), ws, torch.device("cpu"))
+    q.put((r, ws, t))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks_gloo():
+    ctx = torch.multiprocessing.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2, 3.0), (1, 2, 3.0)]
+
+
+def test_reference_arm_prints_oracle_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny_mixed", "--steps", "1", "--warmup", "3", "--ref-budget", "0.2"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["warmup"] >= 3
