@@ -13,9 +13,17 @@
 //               tile's MMAs.
 //   warps 2-5   softmax of Q tile 0; warps 6-9 softmax of Q tile 1.  One thread
 //               per query row (= TMEM lane): masking, online max / sum, P
-//               (rounded to the input type) written over S in TMEM, lazy O
-//               rescaling (only when the running max grows by more than 2^8),
-//               and the epilogue O / l -> out, LSE.
+//               (rounded to the input type) written over S in TMEM in two
+//               halves of 64 keys (the MMA warp starts P V on the first half
+//               while the second is computed), lazy O rescaling (only when the
+//               running max grows by more than 2^8), and the epilogue
+//               O / l -> out, LSE.
+//
+// Each tile's chain softmax(S_t(j)) -> P_t(j) V_j -> S_t(j+1) is serial (P_t
+// lives in S_t's TMEM columns), so throughput comes from interleaving the two
+// tiles: while one tile's softmax runs, the tensor pipe works on the other's
+// MMAs.  K and V stages are released separately: a K stage once both tiles'
+// S MMAs on it are done, a V stage once both P V MMAs are done.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; P_i
 // occupies the first 64 columns of S_i (two 16-bit values per column).
@@ -36,8 +44,8 @@ struct WsSmem {
   alignas(1024) uint8_t k[kWsStages][kTileBytes];
   alignas(1024) uint8_t v[kWsStages][kTileBytes];
   uint64_t q_full, q_empty;
-  uint64_t k_full[kWsStages], v_full[kWsStages], kv_empty[kWsStages];
-  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t k_full[kWsStages], v_full[kWsStages], k_empty[kWsStages], v_empty[kWsStages];
+  uint64_t s_full[2], p_lo[2], p_hi[2], o_full[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -77,9 +85,11 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_smem, uint32_t 
   }
 }
 
+// O += P[:, 16*k0 : 16*k1] V[16*k0 : 16*k1, :]
+template <int k0, int k1>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_smem, uint32_t idesc, bool acc) {
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+  for (int kk = k0; kk < k1; ++kk) {
     // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2048 bytes) of V
     umma_ts(tO, tP + kk * 8, smem_desc_sw128(v_smem + kk * 2048, 16384, 1024), idesc,
             (acc || kk > 0) ? 1u : 0u);
@@ -143,13 +153,16 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
       }
       for (int j = 0; ok && j < g.n_all; ++j) {
         const int st = kv_cnt % kWsStages;
-        if (kv_cnt >= kWsStages) ok = WS_WAIT(&sm.kv_empty[st], ((kv_cnt / kWsStages) - 1) & 1);
+        const uint32_t reuse = ((kv_cnt / kWsStages) - 1) & 1;
+        if (kv_cnt >= kWsStages) ok = WS_WAIT(&sm.k_empty[st], reuse);
         if (!ok) break;
         const int row = s.kv_start + j * kBlockN;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
           tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], g.kvh * p.d + pn * 64, row);
+        if (kv_cnt >= kWsStages) ok = WS_WAIT(&sm.v_empty[st], reuse);
+        if (!ok) break;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
@@ -204,6 +217,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
           umma_commit(&sm.s_full[t]);
         }
       }
+      umma_commit(&sm.k_empty[kv_cnt % kWsStages]);
       if (n == 1) umma_commit(&sm.q_empty);
     }
     bool ok = true;
@@ -214,10 +228,14 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
       const uint32_t vs = smem_u32(sm.v[st]);
       for (int t = 0; t < 2; ++t) {
         if (j >= g.n[t]) continue;
-        if (!WS_WAIT(&sm.p_full[t], p_cnt[t] & 1)) { ok = false; break; }
+        const uint32_t par = p_cnt[t] & 1;
         ++p_cnt[t];
+        if (!WS_WAIT(&sm.p_lo[t], par)) { ok = false; break; }
         tc_fence_after();
-        issue_pv(tO[t], tS[t], vs, idesc_pv, j > 0);
+        issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, j > 0);
+        if (!WS_WAIT(&sm.p_hi[t], par)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
         umma_commit(&sm.o_full[t]);
         if (j + 1 < g.n[t]) {
           if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
@@ -226,8 +244,9 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
           umma_commit(&sm.s_full[t]);
         }
       }
-      if (j == n - 2) umma_commit(&sm.q_empty);   // last S MMAs of the item issued
-      umma_commit(&sm.kv_empty[st]);
+      if (j + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
+      if (j == n - 2) umma_commit(&sm.q_empty);        // last S MMAs of the item issued
+      umma_commit(&sm.v_empty[st]);
     }
     kv_cnt += n;
     if (!ok) break;
@@ -269,8 +288,8 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
     const int qpos = qt0 + row;
 
     float m_run = -INFINITY;
-    float lr[4] = {0.f, 0.f, 0.f, 0.f};   // rounded-P sums (normalise O)
-    float le[4] = {0.f, 0.f, 0.f, 0.f};   // exact sums (LSE)
+    float2 lr_a = make_float2(0.f, 0.f), lr_b = lr_a;   // rounded-P sums (normalise O)
+    float2 le_a = lr_a, le_b = lr_a;                     // exact sums (LSE)
     bool ok = true;
     for (int j = 0; j < ni; ++j) {
       if (!WS_WAIT_WARP(&sm.s_full[tile], s_cnt & 1)) { ok = false; break; }
@@ -291,56 +310,76 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // row max: three-input max, four independent chains
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(sr[c + u]));
+      for (int c = 0; c < 128; c += 8) {
+        mx0 = fmax3f(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+        mx1 = fmax3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mx2 = fmax3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+        mx3 = fmax3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
       }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float m_tile = fmax3f(fmaxf(mx0, mx1), mx2, mx3);
       const float m_new = fmaxf(m_run, m_tile);
       const bool need = (m_new - m_run) * sl2 > kRescaleThreshold;   // false while both are -inf
       float alpha = 1.f;
       if (need) {
         alpha = ex2_approx((m_run - m_new) * sl2);
         m_run = m_new;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          lr[u] *= alpha;
-          le[u] *= alpha;
-        }
+        const float2 a2 = make_float2(alpha, alpha);
+        lr_a = __fmul2_rn(lr_a, a2);
+        lr_b = __fmul2_rn(lr_b, a2);
+        le_a = __fmul2_rn(le_a, a2);
+        le_b = __fmul2_rn(le_b, a2);
       }
       const float mb = (m_run == -INFINITY ? 0.f : m_run) * sl2;
+      const float2 scale2 = make_float2(sl2, sl2);
+      const float2 bias2 = make_float2(-mb, -mb);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+      for (int half = 0; half < 2; ++half) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float x0 = ex2_approx(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -mb));
-          const float x1 = ex2_approx(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -mb));
-          pk[e] = Tr::pack2(x0, x1);
-          le[e & 3] += x0 + x1;
-          lr[e & 3] += Tr::lo(pk[e]) + Tr::hi(pk[e]);
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 arg = __ffma2_rn(
+                make_float2(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1])), scale2,
+                bias2);
+            const float x0 = ex2_approx(arg.x);
+            const float x1 = ex2_approx(arg.y);
+            pk[e] = Tr::pack2(x0, x1);
+            const float2 xr = make_float2(Tr::lo(pk[e]), Tr::hi(pk[e]));
+            if (e & 1) {
+              le_b = __fadd2_rn(le_b, make_float2(x0, x1));
+              lr_b = __fadd2_rn(lr_b, xr);
+            } else {
+              le_a = __fadd2_rn(le_a, make_float2(x0, x1));
+              lr_a = __fadd2_rn(lr_a, xr);
+            }
+          }
+          tmem_st16(tS + 16 * c, pk);
         }
-        tmem_st16(tS + 16 * c, pk);
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_i must hold the previous P V product before it is rescaled
-        if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
+        if (half == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
+          // O_t must hold the previous P V product before it is rescaled, and the
+          // rescaled O must be in TMEM before this tile's first P V step
+          if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < DP / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_ld_wait_regs32(o);
+          for (int c = 0; c < DP / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_ld_wait_regs32(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + 32 * c, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(half == 0 ? &sm.p_lo[tile] : &sm.p_hi[tile]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.p_full[tile]);
+      if (!ok) break;
     }
     if (!ok) break;
     o_cnt += ni;
@@ -351,8 +390,8 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
     if (ni > 0) {
       if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt - 1) & 1)) break;
       tc_fence_after();
-      const float l_r = (lr[0] + lr[1]) + (lr[2] + lr[3]);
-      const float l_e = (le[0] + le[1]) + (le[2] + le[3]);
+      const float l_r = (lr_a.x + lr_a.y) + (lr_b.x + lr_b.y);
+      const float l_e = (le_a.x + le_a.y) + (le_b.x + le_b.y);
       const float inv = 1.f / l_r;
 #pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
@@ -396,11 +435,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     for (int s = 0; s < kWsStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
-      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.p_lo[t], 4);   // one lane of each softmax warp
+      mbar_init(&sm.p_hi[t], 4);
       mbar_init(&sm.o_full[t], 1);
       mbar_init(&sm.item_full[t], 1);
       mbar_init(&sm.item_empty[t], 9);   // MMA thread + one lane of each softmax warp

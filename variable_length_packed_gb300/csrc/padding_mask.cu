@@ -34,8 +34,9 @@ struct MaskArgs {
   int div32;           // total < 2^32: use the reciprocal
 };
 
+// read-only path: the loads of several chunks can be in flight at once
 __device__ __forceinline__ long long row_len(const int32_t* cu, long long b) {
-  return (long long)cu[b + 1] - (long long)cu[b];
+  return (long long)__ldg(cu + b + 1) - (long long)__ldg(cu + b);
 }
 
 __device__ __forceinline__ void div_row(const MaskArgs& a, long long f, long long& b, long long& p) {
@@ -95,13 +96,14 @@ __global__ void __launch_bounds__(256) padding_mask_kernel(const MaskArgs a) {
   uint4* body = reinterpret_cast<uint4*>(a.mask + a.head);
   if (a.S >= 16) {
     long long c = tid;
-    for (; c + stride < a.nchunks; c += 2 * stride) {     // two independent chunks in flight
-      const uint4 v0 = mask_chunk(a, a.head + c * 16);
-      const uint4 v1 = mask_chunk(a, a.head + (c + stride) * 16);
-      body[c] = v0;
-      body[c + stride] = v1;
+    for (; c + 3 * stride < a.nchunks; c += 4 * stride) {   // four independent chunks in flight
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = mask_chunk(a, a.head + (c + u * stride) * 16);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) body[c + u * stride] = v[u];
     }
-    if (c < a.nchunks) body[c] = mask_chunk(a, a.head + c * 16);
+    for (; c < a.nchunks; c += stride) body[c] = mask_chunk(a, a.head + c * 16);
   } else {
     for (long long c = tid; c < a.nchunks; c += stride) {
       uint32_t w[4];
@@ -133,7 +135,7 @@ cudaError_t launch_padding_mask(const int32_t* cu, int B, int S, uint8_t* mask, 
   a.div32 = a.total <= 0xFFFFFFFFll ? 1 : 0;
   a.recip = S > 1 ? (0xFFFFFFFFFFFFFFFFull / (uint64_t)S) + 1ull : 0ull;
   const int threads = 256;
-  long long want = (a.nchunks + 2 * threads - 1) / (2 * threads);
+  long long want = (a.nchunks + 4 * threads - 1) / (4 * threads);
   if (want < 1) want = 1;
   const long long cap = (long long)num_sms * 8;   // 8 resident 256-thread blocks per SM
   const int grid = (int)(want < cap ? want : cap);

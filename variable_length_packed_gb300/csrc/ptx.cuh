@@ -263,6 +263,13 @@ __device__ __forceinline__ void tmem_st_wait() {
 // ----------------------------------------------------------------------------
 // math helpers
 // ----------------------------------------------------------------------------
+// max of three floats in one instruction (PTX max.f32 with three sources).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the hardware approximation (PTX ex2.approx, the MUFU unit);
 // returns 0 for x == -inf.
 __device__ __forceinline__ float ex2_approx(float x) {
