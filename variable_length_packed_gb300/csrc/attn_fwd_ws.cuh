@@ -75,24 +75,28 @@ __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const AttnPara
   return g;
 }
 
+// S = Q K^T over head_dim DP: DP/16 K steps of 16 elements (32 bytes inside a
+// 128-byte swizzle row; the second 64-column panel starts 16 KB further).
+// q_lo / k_lo are the low descriptor words of the tiles' first K step.
 template <int DP>
-__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_smem, uint32_t k_smem, uint32_t idesc) {
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_lo, uint32_t idesc) {
+  constexpr uint32_t hi = smem_desc_sw128_hi(1024);
 #pragma unroll
   for (int kk = 0; kk < DP / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-    umma_ss(tS, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024), idesc,
-            kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+    umma_ss(tS, smem_desc_join(q_lo + off, hi), smem_desc_join(k_lo + off, hi), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O += P[:, 16*k0 : 16*k1] V[16*k0 : 16*k1, :]
+// O += P[:, 16*k0 : 16*k1] V[16*k0 : 16*k1, :].  v_lo is the low descriptor word
+// of the V tile (MN-major: the next 64 head-dim columns are 16 KB further).
 template <int k0, int k1>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_smem, uint32_t idesc, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, uint32_t idesc, bool acc) {
+  constexpr uint32_t hi = smem_desc_sw128_hi(1024);
 #pragma unroll
   for (int kk = k0; kk < k1; ++kk) {
     // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2048 bytes) of V
-    umma_ts(tO, tP + kk * 8, smem_desc_sw128(v_smem + kk * 2048, 16384, 1024), idesc,
-            (acc || kk > 0) ? 1u : 0u);
+    umma_ts(tO, tP + kk * 8, smem_desc_join(v_lo + kk * (2048 >> 4), hi), idesc, (acc || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -194,6 +198,11 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   constexpr uint32_t idesc_pv = umma_idesc_f16(Tr::kBF16, kTileM, DP, true);
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 256 + DP};
+  // low descriptor words; consecutive tiles / stages are kTileBytes apart
+  constexpr uint32_t kStep = WsSmem<DP>::kTileBytes >> 4;
+  const uint32_t q_lo0 = smem_desc_sw128_lo(smem_u32(sm.q[0]), 16);
+  const uint32_t k_lo0 = smem_desc_sw128_lo(smem_u32(sm.k[0]), 16);
+  const uint32_t v_lo0 = smem_desc_sw128_lo(smem_u32(sm.v[0]), 16384);
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, p_cnt[2] = {0, 0};
   for (;;) {
     const int slot = it_cnt & 1;
@@ -210,10 +219,11 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     if (!WS_WAIT(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
     tc_fence_after();
     {
-      const uint32_t ks = smem_u32(sm.k[kv_cnt % kWsStages]);
+      const uint32_t ks = k_lo0 + (kv_cnt % kWsStages) * kStep;
+#pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (g.n[t] > 0) {
-          issue_qk<DP>(tS[t], smem_u32(sm.q[t]), ks, idesc_qk);
+          issue_qk<DP>(tS[t], q_lo0 + t * kStep, ks, idesc_qk);
           umma_commit(&sm.s_full[t]);
         }
       }
@@ -225,7 +235,8 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
       const uint32_t c = kv_cnt + j, cn = c + 1;
       const int st = c % kWsStages, stn = cn % kWsStages;
       if (!WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
-      const uint32_t vs = smem_u32(sm.v[st]);
+      const uint32_t vs = v_lo0 + st * kStep;
+#pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= g.n[t]) continue;
         const uint32_t par = p_cnt[t] & 1;
@@ -240,7 +251,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         if (j + 1 < g.n[t]) {
           if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
           tc_fence_after();
-          issue_qk<DP>(tS[t], smem_u32(sm.q[t]), smem_u32(sm.k[stn]), idesc_qk);
+          issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + stn * kStep, idesc_qk);
           umma_commit(&sm.s_full[t]);
         }
       }

@@ -174,6 +174,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor split in two 32-bit words: the high word holds the fields
+// that do not depend on the tile's address (stride offset, version, swizzle);
+// the low word holds the start address (>> 4) and the leading offset, so moving
+// to another K step or another tile is one 32-bit add.  Addresses stay below
+// 256 KB, so the 14-bit start field never carries into the offset field.
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_sw128_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t smem_desc_join(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // TMEM -> registers, 32 lanes x 32 bits, repeated over 32 consecutive columns.
 // The values are valid only after tmem_ld_wait / tmem_wait_regs.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
