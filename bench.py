@@ -313,6 +313,41 @@ def run_gpu(args, ws, rank, local):
                               "effective_tflops": eff / (attn_ms * 1e-3) / 1e12, "status": status}), flush=True)
         return 0
 
+    # ---- the other packed batches: attention alone, same kernel, inputs drawn on the device ----
+    others = {}
+    for name in args.also:
+        ow = workloads.make(name, tensors=False)
+        oq, ok_, ov = workloads.device_qkv(ow, dev, seed=1)
+        ocu = torch.from_numpy(ow.cu_seqlens).to(dev)
+        opad = None if ow.cu_seqlens_padded is None else torch.from_numpy(ow.cu_seqlens_padded).to(dev)
+        ocz = torch.from_numpy(ow.seq_is_causal).to(dev)
+        oout = torch.empty_like(oq)
+        olse = torch.empty((ow.num_heads_q, ow.total_tokens), dtype=torch.float32, device=dev)
+
+        def ocall():
+            vlp.thd_attn_fwd(oq, ok_, ov, ocu, ocu, opad, opad, ocz, ow.batch_size, ow.max_seqlen,
+                             ow.softmax_scale, out=oout, lse=olse, workspace=wsp)
+        for _ in range(3):
+            ocall()
+        torch.cuda.synchronize()
+        reps = 10
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for _ in range(reps):
+            ocall()
+        o1.record(stream)
+        torch.cuda.synchronize()
+        oms = o0.elapsed_time(o1) / reps
+        oeff = effective_flops(ow)
+        obytes = attn_bytes(ow)
+        others[name] = {"ms_per_launch": oms, "effective_tflops": oeff / (oms * 1e-3) / 1e12,
+                        "frac_of_bf16_peak": oeff / (oms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                        "algorithmic_gbs": obytes / (oms * 1e-3) / 1e9,
+                        "frac_of_hbm": obytes / (oms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "tokens": ow.total_tokens, "batch": ow.batch_size, "heads_q": ow.num_heads_q,
+                        "heads_kv": ow.num_heads_kv, "head_dim": ow.head_dim, "dtype": str(ow.dtype)}
+        del oq, ok_, ov, oout, olse
+
     # ---- padding mask alone on the 4096 x 8192 workload (CUDA graph of back-to-back launches) ----
     mw = workloads.make_mask()
     mcu = torch.from_numpy(mw.cu_seqlens).to(dev)
@@ -400,6 +435,7 @@ def run_gpu(args, ws, rank, local):
                  "timing": f"CUDA graph of {reps} back-to-back launches", "traffic": recorded_traffic("padding_mask")},
         "e2e": {"value": ws * eff / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "other_workloads": others,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.result,
         "device_status_word": status,
@@ -425,6 +461,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS),
                     help="packed batch to run (default: the long-context workload the metric is quoted on)")
+    ap.add_argument("--also", nargs="*", default=["padded_gaps", "mixed_gqa", "many_short"],
+                    help="other packed batches whose attention launch is timed alone (after the step)")
     ap.add_argument("--attn-only", action="store_true",
                     help="run only the attention launches (warm-up + timed) and print the line; "
                          "for profiler captures")

@@ -280,6 +280,12 @@ struct DTypeTraits<__nv_bfloat16> {
   }
   __device__ static __forceinline__ float lo(uint32_t x) { return __uint_as_float(x << 16); }
   __device__ static __forceinline__ float hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+  // a += low half of x, b += high half of x (mixed-precision adds, exact widening)
+  __device__ static __forceinline__ void acc2(uint32_t x, float& a, float& b) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(a), "+f"(b) : "r"(x));
+  }
 };
 template <>
 struct DTypeTraits<__half> {
@@ -293,6 +299,11 @@ struct DTypeTraits<__half> {
   }
   __device__ static __forceinline__ float hi(uint32_t x) {
     return __half2float(__ushort_as_half((unsigned short)(x >> 16)));
+  }
+  __device__ static __forceinline__ void acc2(uint32_t x, float& a, float& b) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+        : "+f"(a), "+f"(b) : "r"(x));
   }
 };
 

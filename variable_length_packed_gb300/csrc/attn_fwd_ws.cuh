@@ -359,13 +359,12 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
             const float x0 = ex2_approx(arg.x);
             const float x1 = ex2_approx(arg.y);
             pk[e] = Tr::pack2(x0, x1);
-            const float2 xr = make_float2(Tr::lo(pk[e]), Tr::hi(pk[e]));
             if (e & 1) {
               le_b = __fadd2_rn(le_b, make_float2(x0, x1));
-              lr_b = __fadd2_rn(lr_b, xr);
+              Tr::acc2(pk[e], lr_b.x, lr_b.y);
             } else {
               le_a = __fadd2_rn(le_a, make_float2(x0, x1));
-              lr_a = __fadd2_rn(lr_a, xr);
+              Tr::acc2(pk[e], lr_a.x, lr_a.y);
             }
           }
           tmem_st16(tS + 16 * c, pk);

@@ -126,8 +126,11 @@ def from_lengths(name, lengths, causal, *, gaps_before=None, trailing=0, heads_q
         with_padded = bool(np.any(np.asarray(gaps_before) != 0) or trailing != 0)
     heads_kv = heads_q if heads_kv is None else heads_kv
     cu, padded, flags = _buffers(lengths, starts, T, causal, capacity, rng)
-    q, k, v = _qkv(seed, T, heads_q, heads_kv, head_dim, dtype)
-    if gap_fill is not None:
+    if _MAKE_TENSORS:
+        q, k, v = _qkv(seed, T, heads_q, heads_kv, head_dim, dtype)
+    else:
+        q = k = v = None
+    if gap_fill is not None and q is not None:
         valid = np.zeros(T, dtype=bool)
         for s, L in zip(starts, lengths):
             valid[s:s + L] = True
@@ -272,8 +275,30 @@ WORKLOADS = {
 }
 
 
-def make(name):
-    return WORKLOADS[name]()
+_MAKE_TENSORS = True
+
+
+def make(name, tensors=True):
+    """Build workload `name`.  With tensors=False only the metadata is drawn (q/k/v are
+    None); device_qkv() then draws same-shaped tensors directly on a GPU."""
+    global _MAKE_TENSORS
+    _MAKE_TENSORS = tensors
+    try:
+        return WORKLOADS[name]()
+    finally:
+        _MAKE_TENSORS = True
+
+
+def device_qkv(w, device, seed=0):
+    """Q/K/V of w's shapes and dtype drawn with a seeded generator on `device`
+    (N(0,1) in fp32, then cast), for timing runs that need no host copy."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    shape_q = (w.total_tokens, w.num_heads_q, w.head_dim)
+    shape_kv = (w.total_tokens, w.num_heads_kv, w.head_dim)
+    q = torch.randn(shape_q, generator=g, device=device, dtype=torch.float32).to(w.dtype)
+    k = torch.randn(shape_kv, generator=g, device=device, dtype=torch.float32).to(w.dtype)
+    v = torch.randn(shape_kv, generator=g, device=device, dtype=torch.float32).to(w.dtype)
+    return q, k, v
 
 
 def make_mask(name="mask_many", seed=4):
