@@ -25,13 +25,24 @@ Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (closed forms, the pages' printed values, a library routine, brute force and
 case counts).  Nothing is "parity unpinned".
 """
-from .attention import thd_attention_fwd, thd_attention_rows, sequence_spans
-from .mask import padding_mask_loop, padding_mask_formula
+from .attention import (thd_attention_fwd, thd_attention_rows, sequence_spans, thd_attention_fwd_general,
+                        merge_partials, visible_keys, MASK_PADDING, MASK_PADDING_CAUSAL,
+                        MASK_PADDING_CAUSAL_BOTTOM_RIGHT)
+from .mask import (padding_mask_loop, padding_mask_formula, padding_mask_cross_loop,
+                   padding_mask_cross_formula)
 
 __all__ = [
     "thd_attention_fwd",
     "thd_attention_rows",
     "sequence_spans",
+    "thd_attention_fwd_general",
+    "merge_partials",
+    "visible_keys",
+    "MASK_PADDING",
+    "MASK_PADDING_CAUSAL",
+    "MASK_PADDING_CAUSAL_BOTTOM_RIGHT",
     "padding_mask_loop",
     "padding_mask_formula",
+    "padding_mask_cross_loop",
+    "padding_mask_cross_formula",
 ]

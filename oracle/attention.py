@@ -132,3 +132,89 @@ def thd_attention_rows(q, k, v, start_q, start_kv, length, causal, head, group,
     e = np.exp(z - zmax)
     s = e.sum(axis=1, keepdims=True)
     return (e / s) @ vv, (zmax + np.log(s))[:, 0]
+
+
+# ---------------------------------------------------------------------------------------------
+# General form: separate query / key-value sequences and a per-sequence mask type.
+# ---------------------------------------------------------------------------------------------
+
+MASK_PADDING = 0                  # every valid key visible
+MASK_PADDING_CAUSAL = 1           # top-left: key j visible to query i iff j <= i
+MASK_PADDING_CAUSAL_BOTTOM_RIGHT = 2   # key j visible iff j <= i + (Lkv - Lq)
+
+
+def visible_keys(i, Lq, Lkv, mask_type):
+    """Number of visible keys (a prefix of the key sequence) for query position i.
+
+    The mask types are the ones the per-sequence policy review comment of "Add
+    per-sequence causal policy to packed THD attention" lists (padding,
+    padding_causal, padding_causal_bottom_right).  Any code other than 0 and 2 means
+    top-left causal, so a boolean flag keeps its meaning.
+    """
+    if mask_type == MASK_PADDING:
+        return Lkv
+    shift = (Lkv - Lq) if mask_type == MASK_PADDING_CAUSAL_BOTTOM_RIGHT else 0
+    return int(min(Lkv, max(0, i + shift + 1)))
+
+
+def thd_attention_fwd_general(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                              cu_seqlens_kv_padded, mask_type, batch_size, softmax_scale):
+    """Packed attention with separate query and key/value sequences.
+
+    Query sequence b is rows [sq_b, sq_b + Lq_b) of q, its key/value sequence rows
+    [sk_b, sk_b + Lkv_b) of k and v (same packing rules as thd_attention_fwd).  Query i
+    sees the first visible_keys(i, ...) keys of its sequence.  Rows that see no key, and
+    rows of no sequence, get out = 0 and lse = -inf.  mask_type: per-sequence codes
+    (None = all MASK_PADDING).  Returns (out [Tq, Hq, d], lse [Hq, Tq]) in fp64.
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    Tq, Hq, d = q.shape
+    group = Hq // k.shape[1]
+    qs, ql = sequence_spans(cu_seqlens_q, cu_seqlens_q_padded, batch_size)
+    ks, kl = sequence_spans(cu_seqlens_kv, cu_seqlens_kv_padded, batch_size)
+    codes = (np.zeros(batch_size, dtype=np.int64) if mask_type is None
+             else np.asarray(mask_type)[:batch_size].astype(np.int64))
+    out = np.zeros((Tq, Hq, d), dtype=np.float64)
+    lse = np.full((Hq, Tq), -np.inf, dtype=np.float64)
+    for b in range(batch_size):
+        Lq, Lkv = int(ql[b]), int(kl[b])
+        if Lq <= 0:
+            continue
+        nvis = np.array([visible_keys(i, Lq, max(Lkv, 0), int(codes[b])) for i in range(Lq)])
+        for h in range(Hq):
+            g = h // group
+            qq = q[qs[b]:qs[b] + Lq, h, :]
+            kk = k[ks[b]:ks[b] + max(Lkv, 0), g, :]
+            vv = v[ks[b]:ks[b] + max(Lkv, 0), g, :]
+            for i in range(Lq):
+                n = nvis[i]
+                if n == 0:
+                    continue
+                z = softmax_scale * (kk[:n] @ qq[i])
+                zmax = z.max()
+                e = np.exp(z - zmax)
+                s = e.sum()
+                out[qs[b] + i, h, :] = (e / s) @ vv[:n]
+                lse[h, qs[b] + i] = zmax + np.log(s)
+    return out, lse
+
+
+def merge_partials(out_a, lse_a, out_b, lse_b):
+    """Attention over the union of two disjoint key sets, from the attention over each.
+
+    With S = exp(lse_a) + exp(lse_b):  lse = log S and
+    out = exp(lse_a - lse) out_a + exp(lse_b - lse) out_b.  A partial with lse = -inf saw no
+    key and has weight 0; when both are -inf the row is out = 0, lse = -inf.  Layouts:
+    out [T, H, d], lse [H, T].  This is the combination the two-call pad_between_seqs
+    example relies on (each call's rows have -inf where the other call has values).
+    """
+    out_a, out_b = _as64(out_a), _as64(out_b)
+    lse_a = np.asarray(lse_a, dtype=np.float64)
+    lse_b = np.asarray(lse_b, dtype=np.float64)
+    lse = np.logaddexp(lse_a, lse_b)
+    both = np.isneginf(lse)
+    safe = np.where(both, 0.0, lse)
+    wa = np.where(np.isneginf(lse_a), 0.0, np.exp(lse_a - safe))
+    wb = np.where(np.isneginf(lse_b), 0.0, np.exp(lse_b - safe))
+    out = wa.T[:, :, None] * out_a + wb.T[:, :, None] * out_b
+    return out, lse

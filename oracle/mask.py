@@ -41,3 +41,15 @@ def padding_mask_formula(cu_seqlens, batch_size, max_seqlen):
     positions = np.arange(max_seqlen, dtype=np.int64)
     mask = positions[None, :] >= seqlens[:, None]
     return mask.reshape(batch_size, 1, 1, max_seqlen)
+
+
+def padding_mask_cross_loop(cu_seqlens_q, cu_seqlens_kv, batch_size, max_seqlen_q, max_seqlen_kv):
+    """Cross-attention form (Equivalence section: q and kv lengths): the pair of masks
+    (query positions, key positions), each built by the old loop."""
+    return (padding_mask_loop(cu_seqlens_q, batch_size, max_seqlen_q),
+            padding_mask_loop(cu_seqlens_kv, batch_size, max_seqlen_kv))
+
+
+def padding_mask_cross_formula(cu_seqlens_q, cu_seqlens_kv, batch_size, max_seqlen_q, max_seqlen_kv):
+    return (padding_mask_formula(cu_seqlens_q, batch_size, max_seqlen_q),
+            padding_mask_formula(cu_seqlens_kv, batch_size, max_seqlen_kv))

@@ -99,3 +99,42 @@ def test_pins_catch_mutant(monkeypatch, target, mutant):
         except (AssertionError, ValueError, IndexError):
             failed += 1
     assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
+
+
+import test_oracle_general as gen
+
+GENERAL_PINS = [
+    gen.test_page1_context_parallel_merge_gives_printed_output,
+    gen.test_two_call_merge_equals_mixed_call,
+    lambda: [gen.test_general_against_torch_sdpa_with_mask(lq, lkv, 2) for lq, lkv in ((5, 9), (9, 5))],
+    gen.test_single_query_bottom_right_sees_every_key,
+    lambda: gen.test_merge_of_key_split_equals_full(13),
+]
+
+
+def bottom_right_sign_flipped(i, Lq, Lkv, mask_type):
+    if mask_type == 0:
+        return Lkv
+    shift = (Lq - Lkv) if mask_type == 2 else 0   # mistake: offset of the wrong sign
+    return int(min(Lkv, max(0, i + shift + 1)))
+
+
+def merge_unweighted(out_a, lse_a, out_b, lse_b):
+    return out_a + out_b, np.logaddexp(lse_a, lse_b)   # mistake: partials not reweighted
+
+
+@pytest.mark.parametrize("target,mutant", [
+    ("visible_keys", bottom_right_sign_flipped),
+    ("merge_partials", merge_unweighted),
+])
+def test_general_pins_catch_mutant(monkeypatch, target, mutant):
+    import oracle as pkg
+    monkeypatch.setattr(oa, target, mutant)
+    monkeypatch.setattr(pkg, target, mutant)
+    failed = 0
+    for pin in GENERAL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
