@@ -75,9 +75,14 @@ size_t thd_attn_workspace_size(void);
  *              valid and the rest, up to the next slot, are pad.  NULL means
  *              sequence b starts at cu_seqlens[b] (no gaps).  Entries past
  *              batch_size - 1 are never read.
- * seq_is_causal device uint8 [>= batch_size] or NULL (all full-context).  Non-zero
- *              selects top-left causal masking (key j visible to query i iff
- *              j <= i, positions counted from the sequence's first token).
+ * seq_is_causal device uint8 [>= batch_size] or NULL (all full-context): the
+ *              per-sequence mask type.  0 = padding (every valid key visible);
+ *              2 = padding_causal_bottom_right (key j visible to query i iff
+ *              j <= i + Lkv - Lq); any other value = padding_causal, top-left
+ *              (j <= i), so a bool tensor works as a causal flag.  Positions
+ *              count from the sequence's first token.  Mask type names: the
+ *              per-sequence policy review comment of the same PR.  Rows that
+ *              see no key are written as 0 with lse -inf.
  * batch_size   >= 0.  0 writes zeros to every row of `out` (and -inf to lse).
  * max_seqlen   >= 0; a sizing hint only (the kernels read the true lengths).
  * softmax_scale finite, > 0.
@@ -157,6 +162,45 @@ int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  */
 int thd_padding_mask(const int32_t* cu_seqlens, int batch_size, int max_seqlen,
                      uint8_t* mask, void* stream);
+
+/*
+ * thd_padding_mask_cross — the cross-attention pair of padding masks: the query
+ * mask from cu_seqlens_q over max_seqlen_q positions and the key/value mask from
+ * cu_seqlens_kv over max_seqlen_kv positions, each exactly as thd_padding_mask.
+ *
+ * Source: "[PyTorch] Build the attention padding mask without host syncs"
+ * (TransformerEngine PR), Equivalence (the cross-attention case: q and kv
+ * lengths per sequence).
+ * Arguments as thd_padding_mask; mask_q is [B*Sq] bytes, mask_kv [B*Skv] bytes.
+ * batch_size 0 launches nothing.  Errors: THD_ERR_ARG, THD_ERR_CUDA.
+ */
+int thd_padding_mask_cross(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch_size,
+                           int max_seqlen_q, int max_seqlen_kv, uint8_t* mask_q, uint8_t* mask_kv,
+                           void* stream);
+
+/*
+ * thd_attn_merge — attention over the union of two disjoint key sets, from the
+ * two partial results: with S = exp(lse_a) + exp(lse_b) per (row, head),
+ * lse = log S and out = exp(lse_a - lse) out_a + exp(lse_b - lse) out_b.  A
+ * partial whose lse is -inf saw no key and gets weight 0; if both are -inf the
+ * row is 0 with lse -inf.
+ *
+ * Source: the context-parallel split of "How to pad sequences that cannot be
+ * evenly split in context parallelism (CP)?" (Megatron-LM issue; each rank's
+ * key chunk gives one partial) and the out_causal + out_non_causal sum of the
+ * pad_between_seqs review comment in "Add per-sequence causal policy to packed
+ * THD attention" (every row has one -inf partial there).
+ *
+ * out_a, out_b, out  device [T, H, head_dim] dtype, 16-byte aligned; out may be
+ *                    out_a or out_b (in place).
+ * lse_a, lse_b, lse  device float32 [H, T]; lse may be lse_a or lse_b.
+ * total_tokens T >= 0 (0 launches nothing), num_heads H >= 1, head_dim a multiple
+ * of 8 in [8, 128], dtype thd_dtype.  The merge is computed in fp32 and rounded
+ * to nearest even.  Errors: THD_ERR_ARG, THD_ERR_UNSUPPORTED, THD_ERR_CUDA.
+ */
+int thd_attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
+                   void* out, float* lse, int total_tokens, int num_heads, int head_dim, int dtype,
+                   void* stream);
 
 /* Human-readable name of a thd_status value (static storage). */
 const char* thd_status_string(int status);

@@ -14,7 +14,8 @@ import os
 
 import torch
 
-__all__ = ["thd_attn_fwd", "thd_attn_fwd_noalloc", "thd_padding_mask", "thd_attn_workspace_size", "thd_status_string",
+__all__ = ["thd_attn_fwd", "thd_attn_fwd_noalloc", "thd_attn_merge", "thd_padding_mask",
+           "thd_padding_mask_cross", "MASK_PADDING", "MASK_PADDING_CAUSAL", "MASK_PADDING_CAUSAL_BOTTOM_RIGHT", "thd_attn_workspace_size", "thd_status_string",
            "ThdError", "library_path", "load_library", "STATUS_WAIT_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,6 +24,8 @@ _LIB = None
 THD_OK, THD_ERR_ARG, THD_ERR_UNSUPPORTED, THD_ERR_CUDA, THD_ERR_WORKSPACE = 0, -1, -2, -3, -4
 THD_BF16, THD_FP16 = 0, 1
 STATUS_WAIT_TIMEOUT = 0x1
+# per-sequence mask type codes accepted in seq_is_causal (a bool tensor is codes 0 / 1)
+MASK_PADDING, MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 
 
 class ThdError(RuntimeError):
@@ -49,6 +52,10 @@ def load_library():
     lib.thd_attn_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P, SZ, P]
     lib.thd_attn_fwd_noalloc.restype = I
     lib.thd_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P]
+    lib.thd_attn_merge.restype = I
+    lib.thd_attn_merge.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
+    lib.thd_padding_mask_cross.restype = I
+    lib.thd_padding_mask_cross.argtypes = [P, P, I, I, I, P, P, P]
     lib.thd_padding_mask.restype = I
     lib.thd_padding_mask.argtypes = [P, I, I, P, P]
     lib.thd_attn_workspace_size.restype = SZ
@@ -94,7 +101,9 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
 
     q: [T, Hq, d], k/v: [T, Hkv, d] (bf16 or fp16, CUDA, contiguous).  cu_seqlens_*:
     int32 CUDA tensors with >= batch_size + 1 entries; *_padded: slot starts or None;
-    seq_is_causal: bool/uint8 CUDA tensor [>= batch_size] or None (all full-context).
+    seq_is_causal: bool/uint8 CUDA tensor [>= batch_size] or None (all full-context), the
+    per-sequence mask type: MASK_PADDING (0), MASK_PADDING_CAUSAL (1, top-left) or
+    MASK_PADDING_CAUSAL_BOTTOM_RIGHT (2).  q and k/v sequences may differ in length.
     Returns (out [T, Hq, d], lse [Hq, T] float32 or None).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
@@ -181,3 +190,52 @@ def thd_padding_mask(cu_seqlens, batch_size, max_seqlen, mask=None):
     if st != THD_OK:
         raise ThdError(st, "thd_padding_mask")
     return mask
+
+
+def thd_attn_merge(out_a, lse_a, out_b, lse_b, out=None, lse=None):
+    """Merge two partial attention results over disjoint key sets (see thd_attn_merge in
+    include/thd_attn.h).  out_*: [T, H, d] bf16/fp16; lse_*: [H, T] float32.  out / lse may
+    be out_a / lse_a (in place)."""
+    for name, t in (("out_a", out_a), ("lse_a", lse_a), ("out_b", out_b), ("lse_b", lse_b),
+                    ("out", out), ("lse", lse)):
+        _cuda(t, name)
+    if out_a.shape != out_b.shape or out_a.dtype != out_b.dtype or out_a.dim() != 3:
+        raise ValueError("out_a and out_b must be [T, H, d] of one dtype")
+    T, H, d = out_a.shape
+    if lse_a.shape != (H, T) or lse_b.shape != (H, T) or lse_a.dtype != torch.float32 \
+            or lse_b.dtype != torch.float32:
+        raise ValueError("lse_a and lse_b must be float32 [H, T]")
+    if out is None:
+        out = torch.empty_like(out_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    with torch.cuda.device(out_a.device):
+        st = _lib().thd_attn_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out), _ptr(lse),
+                                   int(T), int(H), int(d),
+                                   THD_BF16 if out_a.dtype == torch.bfloat16 else THD_FP16,
+                                   _stream_handle(out_a.device))
+    if st != THD_OK:
+        raise ThdError(st, "thd_attn_merge")
+    return out, lse
+
+
+def thd_padding_mask_cross(cu_seqlens_q, cu_seqlens_kv, batch_size, max_seqlen_q, max_seqlen_kv,
+                           mask_q=None, mask_kv=None):
+    """Cross-attention padding masks ([B,1,1,Sq], [B,1,1,Skv]; True = padded position)."""
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv),
+                    ("mask_q", mask_q), ("mask_kv", mask_kv)):
+        _cuda(t, name)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_kv.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    dev = cu_seqlens_q.device
+    if mask_q is None:
+        mask_q = torch.empty((batch_size, 1, 1, max_seqlen_q), dtype=torch.bool, device=dev)
+    if mask_kv is None:
+        mask_kv = torch.empty((batch_size, 1, 1, max_seqlen_kv), dtype=torch.bool, device=dev)
+    with torch.cuda.device(dev):
+        st = _lib().thd_padding_mask_cross(_ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), int(batch_size),
+                                           int(max_seqlen_q), int(max_seqlen_kv), _ptr(mask_q), _ptr(mask_kv),
+                                           _stream_handle(dev))
+    if st != THD_OK:
+        raise ThdError(st, "thd_padding_mask_cross")
+    return mask_q, mask_kv

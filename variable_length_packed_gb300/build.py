@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libthdattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["thd_attn.cu", "padding_mask.cu", "attn_noalloc.cu"]
+SOURCES = ["thd_attn.cu", "padding_mask.cu", "attn_noalloc.cu", "attn_merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -45,8 +45,17 @@ struct AttnParams {
   float scale_log2;        // softmax scale * log2(e)
 };
 
+// Per-sequence mask type codes (the padding / padding_causal /
+// padding_causal_bottom_right types of the per-sequence policy review): 0 =
+// every valid key visible, 2 = bottom-right causal (key j visible to query i
+// iff j <= i + kv_len - q_len), any other non-zero code = top-left causal
+// (j <= i), so a boolean per-sequence flag keeps its meaning.
+constexpr int kMaskPadding = 0;
+constexpr int kMaskCausalBottomRight = 2;
+
 struct SeqInfo {
   int q_start, kv_start, q_len, kv_len, causal;
+  int shift;   // causal visibility offset: key j visible to query i iff j <= i + shift
 };
 
 // Sequence b's rows, clamped to the packed buffer [0, T): garbage metadata
@@ -66,19 +75,21 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
   s.kv_start = (int)ks;
   s.q_len = (int)ql;
   s.kv_len = (int)kl;
-  s.causal = p.causal ? (p.causal[b] != 0) : 0;
+  const int code = p.causal ? (int)p.causal[b] : kMaskPadding;
+  s.causal = code != kMaskPadding;
+  s.shift = code == kMaskCausalBottomRight ? s.kv_len - s.q_len : 0;
   return s;
 }
 
 // Number of KV tiles a Q tile whose first row is sequence position q0 must
-// visit: all keys for a full-context sequence, keys up to the tile's last
-// valid row for a causal one (top-left alignment: key j visible iff j <= i).
+// visit: all keys for a full-context sequence, keys up to the last key visible
+// to the tile's last valid row for a causal one.  0 when no row sees a key.
 __device__ __forceinline__ int kv_tiles_for(const SeqInfo& s, int q0, int rows) {
   if (s.kv_len <= 0) return 0;
   int last = s.kv_len - 1;
   if (s.causal) {
-    int qlast = min(q0 + rows, s.q_len) - 1;
-    last = min(last, qlast);
+    const long long qlast = (long long)min(q0 + rows, s.q_len) - 1 + s.shift;
+    last = (int)(qlast < last ? qlast : last);
     if (last < 0) return 0;
   }
   return last / kBlockN + 1;

@@ -171,14 +171,14 @@ __global__ void __launch_bounds__(128, 1)
         tmem_tie_regs32(sr + 64);
         tmem_tie_regs32(sr + 96);
 
-        const bool need_mask = (kv0 + kBlockN > s.kv_len) || (s.causal && kv0 + kBlockN - 1 > q0);
+        const bool need_mask = (kv0 + kBlockN > s.kv_len) || (s.causal && kv0 + kBlockN - 1 > q0 + s.shift);
         float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           float x = __uint_as_float(sr[c]);
           if (need_mask) {
             const int kp = kv0 + c;
-            const bool ok = kp < s.kv_len && (!s.causal || kp <= qpos);
+            const bool ok = kp < s.kv_len && (!s.causal || kp <= qpos + s.shift);
             x = ok ? x : -INFINITY;
             sr[c] = __float_as_uint(x);
           }
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(128, 1)
     const size_t orow = ((size_t)(s.q_start + (row_ok ? qpos : 0)) * p.Hq + it.h) * (size_t)p.d;
     DT* dst = static_cast<DT*>(p.out) + orow;
     if (nkv > 0) {
-      const float inv = 1.f / l_run;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // a row that saw no key stays 0
 #pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
         uint32_t o[32];

@@ -315,8 +315,9 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
       tmem_tie_regs32(sr + 96);
 
       const int kv0 = j * kBlockN;
-      if (kv0 + kBlockN > s.kv_len || (s.causal && kv0 + kBlockN - 1 > qt0)) {
-        const int lim = s.causal ? min(s.kv_len - 1, qpos) - kv0 : s.kv_len - 1 - kv0;   // last visible column
+      if (kv0 + kBlockN > s.kv_len || (s.causal && kv0 + kBlockN - 1 > qt0 + s.shift)) {
+        // last visible column of this tile for this row (negative: none)
+        const int lim = s.causal ? min(s.kv_len - 1, qpos + s.shift) - kv0 : s.kv_len - 1 - kv0;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
@@ -402,7 +403,7 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
       tc_fence_after();
       const float l_r = (lr_a.x + lr_a.y) + (lr_b.x + lr_b.y);
       const float l_e = (le_a.x + le_a.y) + (le_b.x + le_b.y);
-      const float inv = 1.f / l_r;
+      const float inv = l_r > 0.f ? 1.f / l_r : 0.f;   // a row that saw no key stays 0
 #pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
         uint32_t o[32];

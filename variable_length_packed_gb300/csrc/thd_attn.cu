@@ -15,6 +15,9 @@
 
 namespace thd {
 cudaError_t launch_padding_mask(const int32_t* cu, int B, int S, uint8_t* mask, int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
+                              void* out, float* lse, int T, int H, int d, bool bf16, int num_sms,
+                              cudaStream_t stream);
 }
 
 namespace {
@@ -113,6 +116,35 @@ int thd_padding_mask(const int32_t* cu_seqlens, int batch_size, int max_seqlen, 
   if (sms <= 0) return THD_ERR_CUDA;
   cudaError_t e = thd::launch_padding_mask(cu_seqlens, batch_size, max_seqlen, mask, sms,
                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? THD_OK : THD_ERR_CUDA;
+}
+
+int thd_padding_mask_cross(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch_size,
+                           int max_seqlen_q, int max_seqlen_kv, uint8_t* mask_q, uint8_t* mask_kv, void* stream) {
+  if (batch_size < 0 || max_seqlen_q < 0 || max_seqlen_kv < 0) return THD_ERR_ARG;
+  if (batch_size == 0) return THD_OK;
+  if ((max_seqlen_q > 0 && (!cu_seqlens_q || !mask_q)) || (max_seqlen_kv > 0 && (!cu_seqlens_kv || !mask_kv)))
+    return THD_ERR_ARG;
+  if ((cu_seqlens_q && !aligned(cu_seqlens_q, 4)) || (cu_seqlens_kv && !aligned(cu_seqlens_kv, 4))) return THD_ERR_ARG;
+  int st = thd_padding_mask(cu_seqlens_q, batch_size, max_seqlen_q, mask_q, stream);
+  if (st != THD_OK) return st;
+  return thd_padding_mask(cu_seqlens_kv, batch_size, max_seqlen_kv, mask_kv, stream);
+}
+
+int thd_attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b, void* out,
+                   float* lse, int total_tokens, int num_heads, int head_dim, int dtype, void* stream) {
+  if (total_tokens < 0 || num_heads < 1) return THD_ERR_ARG;
+  if (dtype != THD_BF16 && dtype != THD_FP16) return THD_ERR_UNSUPPORTED;
+  if (head_dim < 8 || head_dim > 128 || head_dim % 8 != 0) return THD_ERR_UNSUPPORTED;
+  if ((long long)total_tokens * num_heads >= (1ll << 40)) return THD_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return THD_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse) return THD_ERR_ARG;
+  if (!aligned(out_a, 16) || !aligned(out_b, 16) || !aligned(out, 16)) return THD_ERR_ARG;
+  if (!aligned(lse_a, 4) || !aligned(lse_b, 4) || !aligned(lse, 4)) return THD_ERR_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return THD_ERR_CUDA;
+  cudaError_t e = thd::launch_attn_merge(out_a, lse_a, out_b, lse_b, out, lse, total_tokens, num_heads, head_dim,
+                                         dtype == THD_BF16, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? THD_OK : THD_ERR_CUDA;
 }
 

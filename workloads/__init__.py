@@ -312,3 +312,22 @@ def make_mask(name="mask_many", seed=4):
     cu[1:] = np.cumsum(lengths)
     return MaskWorkload(name=name, batch_size=B, max_seqlen=S, lengths=lengths,
                         cu_seqlens=cu.astype(np.int32))
+
+
+def merge_inputs(T, H, d, dtype, seed):
+    """Two partial attention results for merge tests: out_* uniform in [-2, 2] ([T, H, d],
+    dtype), lse_* ~ N(0, 3^2) ([H, T], float32); about 5 % of (head, row) entries have
+    lse_a = -inf, 5 % lse_b = -inf and 2 % both, with the matching out rows zero."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    out_a = (torch.rand((T, H, d), generator=g) * 4 - 2).to(dtype)
+    out_b = (torch.rand((T, H, d), generator=g) * 4 - 2).to(dtype)
+    lse_a = torch.randn((H, T), generator=g) * 3
+    lse_b = torch.randn((H, T), generator=g) * 3
+    u = torch.rand((H, T), generator=g)
+    none_a = u < 0.05
+    none_b = (u >= 0.05) & (u < 0.10)
+    both = (u >= 0.10) & (u < 0.12)
+    for lse, out, m in ((lse_a, out_a, none_a | both), (lse_b, out_b, none_b | both)):
+        lse[m] = float("-inf")
+        out.permute(1, 0, 2)[m] = 0
+    return out_a, lse_a, out_b, lse_b
