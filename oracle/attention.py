@@ -38,7 +38,7 @@ import numpy as np
 
 def _as64(x):
     if hasattr(x, "detach"):  # torch tensor -> numpy without importing torch here
-        x = x.detach().cpu().float().numpy()
+        x = x.detach().cpu().double().numpy()
     return np.asarray(x, dtype=np.float64)
 
 
@@ -218,3 +218,58 @@ def merge_partials(out_a, lse_a, out_b, lse_b):
     wb = np.where(np.isneginf(lse_b), 0.0, np.exp(lse_b - safe))
     out = wa.T[:, :, None] * out_a + wb.T[:, :, None] * out_b
     return out, lse
+
+
+# ---------------------------------------------------------------------------------------------
+# Backward: gradients of the packed attention with respect to Q, K and V.
+# ---------------------------------------------------------------------------------------------
+
+def thd_attention_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                      cu_seqlens_kv_padded, mask_type, batch_size, softmax_scale):
+    """dQ, dK, dV of out = softmax(scale q k^T [masked]) v for every sequence and head.
+
+    "Add per-sequence causal policy to packed THD attention" (Changes, Validation) checks
+    Q/K/V gradient parity against scalar-policy attention; this is the gradient of the
+    forward defined above, written out from the chain rule (fp64):
+
+        P = softmax(Z) row-wise, Z = scale q k^T with invisible keys at -inf
+        dV = P^T dO,  dP = dO V^T,  dZ = P * (dP - rowsum(P * dP)),
+        dQ = scale dZ K,  dK = scale dZ^T Q.
+
+    Grouped-query heads: dK / dV of a key/value head sum the contributions of every query
+    head that reads it.  Rows of no sequence, rows that see no key and keys no query sees
+    get zero gradient.  Returns (dq [Tq,Hq,d], dk [Tkv,Hkv,d], dv [Tkv,Hkv,d]) in fp64.
+    """
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    Tq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    group = Hq // Hkv
+    qs, ql = sequence_spans(cu_seqlens_q, cu_seqlens_q_padded, batch_size)
+    ks, kl = sequence_spans(cu_seqlens_kv, cu_seqlens_kv_padded, batch_size)
+    codes = (np.zeros(batch_size, dtype=np.int64) if mask_type is None
+             else np.asarray(mask_type)[:batch_size].astype(np.int64))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(batch_size):
+        Lq, Lkv = int(ql[b]), int(kl[b])
+        if Lq <= 0 or Lkv <= 0:
+            continue
+        nvis = np.array([visible_keys(i, Lq, Lkv, int(codes[b])) for i in range(Lq)])
+        visible = np.arange(Lkv)[None, :] < nvis[:, None]
+        rows = nvis > 0
+        sq, sk = slice(qs[b], qs[b] + Lq), slice(ks[b], ks[b] + Lkv)
+        for h in range(Hq):
+            g = h // group
+            Q, K, V, dO = q[sq, h, :], k[sk, g, :], v[sk, g, :], dout[sq, h, :]
+            Z = np.where(visible, softmax_scale * (Q @ K.T), -np.inf)
+            P = np.zeros_like(Z)
+            Zr = Z[rows]
+            E = np.exp(Zr - Zr.max(axis=1, keepdims=True))
+            P[rows] = E / E.sum(axis=1, keepdims=True)
+            dP = dO @ V.T
+            dZ = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dq[sq, h, :] = softmax_scale * (dZ @ K)
+            dk[sk, g, :] += softmax_scale * (dZ.T @ Q)
+            dv[sk, g, :] += P.T @ dO
+    return dq, dk, dv
