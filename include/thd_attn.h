@@ -112,6 +112,49 @@ int thd_attn_fwd(const void* q, const void* k, const void* v,
                  int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * thd_attn_bwd_workspace_size — bytes of device workspace thd_attn_bwd needs for
+ * T = total_tokens rows, Hq query heads and head_dim d:
+ * 256 + (Hq*T*4 rounded up to 256) + (T*Hq*d*4 rounded up to 256); 0 for invalid sizes.
+ * Layout: work counter and status word as in thd_attn_workspace_size, then
+ * D = rowsum(dO * O) (fp32 [Hq, T]), then the fp32 dQ accumulator [T, Hq, d].
+ */
+size_t thd_attn_bwd_workspace_size(int total_tokens, int num_heads_q, int head_dim);
+
+/*
+ * thd_attn_bwd — gradients dQ, dK, dV of thd_attn_fwd, for the same packed
+ * batch, gaps, per-sequence mask types and grouped heads.
+ *
+ * Source: "Add per-sequence causal policy to packed THD attention"
+ * (TransformerEngine PR, Changes and Validation: forward and Q/K/V gradient
+ * parity of mixed, all-causal and all-full packed batches).  With
+ * P = exp(scale q k^T - lse): dV = P^T dO; dS = P * (dO V^T - D),
+ * D = rowsum(dO * O); dQ = scale dS K; dK = scale dS^T Q; dK / dV of a
+ * key/value head sum over the query heads that read it.
+ *
+ * q, k, v, out, lse   the forward's inputs and outputs (out and lse exactly as
+ *                     thd_attn_fwd returned them; lse required).
+ * dout                device [T, Hq, head_dim], dtype: gradient of out.
+ * dq, dk, dv          device, shapes of q, k, v, dtype, 16-byte aligned.  Rows
+ *                     of no sequence, queries that see no key and keys that no
+ *                     query sees get exact zeros.
+ * Other arguments as thd_attn_fwd, except: head_dim 64 or 128 only; workspace
+ * of at least thd_attn_bwd_workspace_size(T, Hq, head_dim) bytes, 256-byte
+ * aligned, needs no initialisation and must not be shared by calls that
+ * overlap on the GPU.
+ * Runs three kernels on `stream` (row sums, the main pass, dQ conversion); no
+ * host synchronisation.  Errors as thd_attn_fwd.
+ */
+int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                 const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                 const uint8_t* seq_is_causal,
+                 int batch_size, int max_seqlen, float softmax_scale,
+                 void* dq, void* dk, void* dv,
+                 int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                 int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * thd_attn_fwd_noalloc — thd_attn_fwd for callers that cannot allocate device
  * memory: identical arguments minus the workspace, identical results.
  *

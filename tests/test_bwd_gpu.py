@@ -1,0 +1,133 @@
+"""thd_attn_bwd on the GPU against the fp64 backward oracle (dQ, dK, dV).
+
+The oracle's gradients come from the inputs (q, k, v, dO) alone; the GPU backward
+consumes the GPU forward's out and lse, as a training step would.
+
+Tolerance (no bound is stated for gradients; derived here): every gradient element is a
+sum over up to L terms in which P or dS was rounded to the input type (relative 2^-9 for
+bf16, 2^-12 for fp16) and the result is rounded once more.  The error is therefore measured
+relative to the largest reference magnitude of that tensor: max |err| <= 2e-2 * max |ref|
+for bf16 and 4e-3 * max |ref| for fp16, i.e. a few units of the input type's rounding at the
+tensor's scale.  Exact zeros are required wherever the gradient is structurally zero.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from thd_testutil import to_device, valid_rows
+
+pytestmark = pytest.mark.gpu
+vlp = pytest.importorskip("variable_length_packed_gb300")
+
+REL = {torch.bfloat16: 2e-2, torch.float16: 4e-3}
+
+
+def run_bwd(w, seed, codes=None, cu_kv=None, pad_q=None, pad_kv=None):
+    dev = to_device(w)
+    causal = dev["causal"] if codes is None else torch.from_numpy(codes).cuda()
+    cu_q = dev["cu"]
+    cu_k = cu_q if cu_kv is None else torch.from_numpy(cu_kv).cuda()
+    pq = dev["padded"] if pad_q is None else torch.from_numpy(pad_q).cuda()
+    pk = dev["padded"] if pad_kv is None else torch.from_numpy(pad_kv).cuda()
+    out, lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], cu_q, cu_k, pq, pk, causal, w.batch_size,
+                                w.max_seqlen, w.softmax_scale)
+    dout = workloads.grad_output(w, seed)
+    dq, dk, dv = vlp.thd_attn_bwd(dev["q"], dev["k"], dev["v"], out, lse, dout.cuda(), cu_q, cu_k, pq, pk, causal,
+                                  w.batch_size, w.max_seqlen, w.softmax_scale)
+    torch.cuda.synchronize()
+    ref = oracle.thd_attention_bwd(w.q, w.k, w.v, dout, cu_q.cpu().numpy(), cu_k.cpu().numpy(),
+                                   None if pq is None else pq.cpu().numpy(), None if pk is None else pk.cpu().numpy(),
+                                   causal.cpu().numpy(), w.batch_size, w.softmax_scale)
+    return (dq, dk, dv), ref
+
+
+def structural_zero_rows(T, cu_q, cu_kv, pad_q, pad_kv, codes, batch):
+    """Rows whose gradient is zero by construction: query rows of no sequence or that see no
+    key (dQ), key rows of no sequence or that no query sees (dK, dV)."""
+    qs, ql = oracle.sequence_spans(cu_q, pad_q, batch)
+    ks, kl = oracle.sequence_spans(cu_kv, pad_kv, batch)
+    zq = np.ones(T, bool)
+    zk = np.ones(T, bool)
+    for b in range(batch):
+        Lq, Lkv = int(ql[b]), int(kl[b])
+        code = 0 if codes is None else int(codes[b])
+        if Lq <= 0 or Lkv <= 0:
+            continue
+        nv = np.array([oracle.visible_keys(i, Lq, Lkv, code) for i in range(Lq)])
+        zq[qs[b]:qs[b] + Lq] = nv == 0
+        zk[ks[b]:ks[b] + nv.max()] = False
+    return zq, zk
+
+
+def check(w, got, ref, name, zeros=None):
+    report, fails = [], []
+    for g, r, label in zip(got, ref, ("dq", "dk", "dv")):
+        g = g.float().cpu().double().numpy()
+        scale = np.abs(r).max()
+        err = np.abs(g - r).max()
+        report.append(f"{name} {label}: max|err| {err:.3e} max|ref| {scale:.3e} rel {err / max(scale, 1e-30):.3e}")
+        if err > REL[w.dtype] * scale + 1e-6:
+            fails.append(report[-1])
+        if zeros is not None:
+            z = zeros[0] if label == "dq" else zeros[1]
+            if not np.all(g[z] == 0):
+                fails.append(f"{name} {label}: structural zeros not exact")
+    print("\n".join(report))
+    assert not fails, fails
+
+
+def layout_zeros(w):
+    return structural_zero_rows(w.total_tokens, w.cu_seqlens, w.cu_seqlens, w.cu_seqlens_padded,
+                                w.cu_seqlens_padded, w.seq_is_causal, w.batch_size)
+
+
+@pytest.mark.parametrize("name", ["tiny_mixed", "padded_gaps"])
+def test_small_workloads(name):
+    w = workloads.make(name)
+    got, ref = run_bwd(w, seed=7)
+    check(w, got, ref, name, layout_zeros(w))
+
+
+@pytest.mark.parametrize("d,dtype,group", [(64, torch.bfloat16, 1), (128, torch.bfloat16, 4), (64, torch.float16, 2),
+                                           (128, torch.float16, 1)])
+def test_mixed_lengths_and_groups(d, dtype, group):
+    lens = [1, 127, 128, 129, 300, 5]
+    causal = [1, 0, 1, 0, 1, 0]
+    w = workloads.from_lengths("bwdmix", lens, causal, gaps_before=[3, 0, 64, 1, 7, 2], trailing=5, heads_q=4,
+                               heads_kv=4 // group, head_dim=d, dtype=dtype, seed=d + group)
+    got, ref = run_bwd(w, seed=3)
+    check(w, got, ref, f"mix d{d} g{group}", layout_zeros(w))
+
+
+def test_mask_types_separate_q_kv():
+    import test_merge_gpu as tm
+    w, cu_q, cu_k, qs, ks, codes = tm.rect_batch(128, torch.bfloat16, seed=5)
+    w.batch_size = 5
+    w.cu_seqlens = cu_q
+    got, ref = run_bwd(w, seed=11, codes=codes, cu_kv=cu_k, pad_q=qs, pad_kv=ks)
+    check(w, got, ref, "rect", structural_zero_rows(w.total_tokens, cu_q, cu_k, qs, ks, codes, 5))
+
+
+def test_mixed_gqa_sampled_sequences():
+    """The 64-sequence GQA batch on the GPU; the oracle computes the gradients of four
+    sequences (each sequence's gradients depend on that sequence only)."""
+    w = workloads.make("mixed_gqa")
+    dev = to_device(w)
+    out, lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"], dev["padded"],
+                                dev["causal"], w.batch_size, w.max_seqlen, w.softmax_scale)
+    dout = workloads.grad_output(w, 13)
+    dq, dk, dv = vlp.thd_attn_bwd(dev["q"], dev["k"], dev["v"], out, lse, dout.cuda(), dev["cu"], dev["cu"],
+                                  dev["padded"], dev["padded"], dev["causal"], w.batch_size, w.max_seqlen,
+                                  w.softmax_scale)
+    torch.cuda.synchronize()
+    order = np.argsort(-w.lengths)
+    for b in [int(order[0]), int(order[1]), int(order[-1]), 17]:
+        s, L = int(w.starts[b]), int(w.lengths[b])
+        sub = slice(s, s + L)
+        ref = oracle.thd_attention_bwd(w.q[sub], w.k[sub], w.v[sub], dout[sub], [0, L], [0, L], None, None,
+                                       [int(w.causal[b])], 1, w.softmax_scale)
+        check(w, (dq[sub], dk[sub], dv[sub]), ref, f"gqa b={b} L={L}")
+    pad = torch.from_numpy(~valid_rows(w)).cuda()
+    assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)

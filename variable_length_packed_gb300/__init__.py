@@ -14,7 +14,7 @@ import os
 
 import torch
 
-__all__ = ["thd_attn_fwd", "thd_attn_fwd_noalloc", "thd_attn_merge", "thd_padding_mask",
+__all__ = ["thd_attn_fwd", "thd_attn_bwd", "thd_attn_fwd_noalloc", "thd_attn_merge", "thd_padding_mask",
            "thd_padding_mask_cross", "MASK_PADDING", "MASK_PADDING_CAUSAL", "MASK_PADDING_CAUSAL_BOTTOM_RIGHT", "thd_attn_workspace_size", "thd_status_string",
            "ThdError", "library_path", "load_library", "STATUS_WAIT_TIMEOUT"]
 
@@ -52,6 +52,10 @@ def load_library():
     lib.thd_attn_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P, SZ, P]
     lib.thd_attn_fwd_noalloc.restype = I
     lib.thd_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P]
+    lib.thd_attn_bwd.restype = I
+    lib.thd_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, F, P, P, P, I, I, I, I, I, P, SZ, P]
+    lib.thd_attn_bwd_workspace_size.restype = SZ
+    lib.thd_attn_bwd_workspace_size.argtypes = [I, I, I]
     lib.thd_attn_merge.restype = I
     lib.thd_attn_merge.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.thd_padding_mask_cross.restype = I
@@ -239,3 +243,40 @@ def thd_padding_mask_cross(cu_seqlens_q, cu_seqlens_kv, batch_size, max_seqlen_q
     if st != THD_OK:
         raise ThdError(st, "thd_padding_mask_cross")
     return mask_q, mask_kv
+
+
+def thd_attn_bwd(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
+                 cu_seqlens_kv_padded=None, seq_is_causal=None, batch_size=None, max_seqlen=0,
+                 softmax_scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """Gradients (dq, dk, dv) of thd_attn_fwd for the same batch; out / lse are the forward's
+    outputs.  head_dim 64 or 128."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout),
+                    ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv),
+                    ("cu_seqlens_q_padded", cu_seqlens_q_padded),
+                    ("cu_seqlens_kv_padded", cu_seqlens_kv_padded), ("seq_is_causal", seq_is_causal),
+                    ("dq", dq), ("dk", dk), ("dv", dv), ("workspace", workspace)):
+        _cuda(t, name)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if out.shape != q.shape or dout.shape != q.shape or lse.shape != (Hq, T) or lse.dtype != torch.float32:
+        raise ValueError("out / dout must match q; lse must be float32 [Hq, T]")
+    if batch_size is None:
+        batch_size = cu_seqlens_q.numel() - 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(_lib().thd_attn_bwd_workspace_size(int(T), int(Hq), int(d)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = _lib().thd_attn_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+            _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), _ptr(seq_is_causal), int(batch_size),
+            int(max_seqlen), float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), int(T), int(Hq), int(Hkv), int(d),
+            THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16, _ptr(workspace), workspace.numel(),
+            _stream_handle(q.device))
+    if st != THD_OK:
+        raise ThdError(st, "thd_attn_bwd")
+    return dq, dk, dv

@@ -128,9 +128,14 @@ __device__ __forceinline__ uint32_t seq_sort_key(const SeqInfo& s) {
   return (uint32_t)(nkv * 2 + (s.causal ? 0 : 1));
 }
 
-template <int BLOCK_M>
-__device__ __forceinline__ uint32_t seq_items(const SeqInfo& s, int Hq) {
-  return s.q_len > 0 ? (uint32_t)((s.q_len + BLOCK_M - 1) / BLOCK_M) * (uint32_t)Hq : 0u;
+// Items of one sequence: blocks of BLOCK rows of the query sequence times the
+// query heads (forward), or of the key/value sequence times the key/value heads
+// (backward, kKvSide).
+template <int BLOCK, bool kKvSide>
+__device__ __forceinline__ uint32_t seq_items(const SeqInfo& s, const AttnParams& p) {
+  const int len = kKvSide ? s.kv_len : s.q_len;
+  const int heads = kKvSide ? p.Hkv : p.Hq;
+  return len > 0 ? (uint32_t)((len + BLOCK - 1) / BLOCK) * (uint32_t)heads : 0u;
 }
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
@@ -144,7 +149,7 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
 }
 
 // Load and sort the chunk of sequences starting at `base`.  One full warp.
-template <int BLOCK_M>
+template <int BLOCK_M, bool kKvSide = false>
 __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   const int lane = threadIdx.x & 31;
   const int n = min(kSchedChunk, p.B - base);
@@ -185,7 +190,7 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   uint32_t carry = 0;
   for (int j0 = 0; j0 < n; j0 += 32) {
     const int j = j0 + lane;
-    const uint32_t it = j < n ? seq_items<BLOCK_M>(load_seq(p, base + s.order[j]), p.Hq) : 0u;
+    const uint32_t it = j < n ? seq_items<BLOCK_M, kKvSide>(load_seq(p, base + s.order[j]), p) : 0u;
     const uint32_t incl = warp_incl_scan(it);
     if (j < n) s.cum[j + 1] = carry + incl;
     carry += __shfl_sync(0xffffffffu, incl, 31);
@@ -205,9 +210,12 @@ struct WorkItem {
   SeqInfo seq;
 };
 
-// One full warp.  Maps global item index w to (sequence, head, query block),
-// loading later chunks as needed (w never decreases within a CTA).
-template <int BLOCK_M>
+// One full warp.  Maps global item index w to (sequence, head, block), loading
+// later chunks as needed (w never decreases within a CTA).  Forward: query
+// blocks, heaviest (last) first; backward (kKvSide): key/value blocks and
+// heads, lowest block first (under causal masking the first keys are seen by
+// the most queries).
+template <int BLOCK_M, bool kKvSide = false>
 __device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
   WorkItem it;
   it.valid = 0;
@@ -215,7 +223,7 @@ __device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned lon
     const int next = s.chunk_base + s.chunk_n;
     if (next >= p.B) return it;
     const unsigned long long base_items = s.item_end;
-    sched_load_chunk<BLOCK_M>(s, p, next);
+    sched_load_chunk<BLOCK_M, kKvSide>(s, p, next);
     if ((threadIdx.x & 31) == 0) {
       s.item_base = base_items;
       s.item_end = base_items + s.cum[s.chunk_n];
@@ -231,9 +239,10 @@ __device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned lon
   it.b = s.chunk_base + s.order[lo];
   it.seq = load_seq(p, it.b);
   const uint32_t r = local - s.cum[lo];
-  const uint32_t nblk = (uint32_t)((it.seq.q_len + BLOCK_M - 1) / BLOCK_M);
+  const int len = kKvSide ? it.seq.kv_len : it.seq.q_len;
+  const uint32_t nblk = (uint32_t)((len + BLOCK_M - 1) / BLOCK_M);
   it.h = (int)(r / nblk);
-  it.qblock = (int)(nblk - 1u - (r % nblk));
+  it.qblock = kKvSide ? (int)(r % nblk) : (int)(nblk - 1u - (r % nblk));
   it.valid = 1;
   return it;
 }
@@ -278,6 +287,13 @@ __device__ void zero_pad_rows(const AttnParams& p, int t0, int nthreads, int ele
       }
     }
   }
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` of a 128-row tile stored as
+// 64-column panels of 16 KB (128-byte rows) with the 128-byte swizzle: the
+// chunk index is XORed with (row mod 8), as TMA writes it.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return (uint32_t)((c >> 3) * (kTileM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <typename DT>

@@ -25,13 +25,6 @@ struct SerialSmem {
   SchedSmem sched;
 };
 
-// Byte offset of 16-byte chunk `c` of row `r` in a K-major (row = 128 bytes of
-// 64 halves per 16 KB panel) tile with the 128-byte swizzle: chunk index XOR
-// (row mod 8).
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
-  return (uint32_t)((c >> 3) * (kTileM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
 // Plain vector loads of a 128-row tile (rows row0.., head column col0) into
 // the swizzled layout; chunks past d and rows outside [0, T) are zero.
 template <int DP>

@@ -159,6 +159,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(bool bf16, int M, int N, b
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Same, with A also selectable as MN-major (A read as its transpose).
+__host__ __device__ constexpr uint32_t umma_idesc_f16_ab(bool bf16, int M, int N, bool a_mn_major,
+                                                         bool b_mn_major) {
+  return umma_idesc_f16(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, for tiles whose 8-row
 // swizzle atoms (1024 bytes) start on 1024-byte boundaries.
 //   lbo: byte distance between atoms adjacent in the leading dimension

@@ -12,6 +12,7 @@
 #include "../../include/thd_attn.h"
 #include "attn_fwd_serial.cuh"
 #include "attn_fwd_ws.cuh"
+#include "attn_bwd.cuh"
 
 namespace thd {
 cudaError_t launch_padding_mask(const int32_t* cu, int B, int S, uint8_t* mask, int num_sms, cudaStream_t stream);
@@ -79,20 +80,134 @@ int launch_serial(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
   return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
 }
 
+// Kernels that allocate all 512 TMEM columns must run one CTA per SM: a second
+// CTA on the same SM would wait in tcgen05.alloc until the first one exits.
+// Requesting more than half of the SM's shared memory guarantees that.
+constexpr size_t kOneCtaPerSmSmem = 120 * 1024;
+size_t one_cta_per_sm(size_t bytes) { return bytes > kOneCtaPerSmSmem ? bytes : kOneCtaPerSmSmem; }
+
 template <typename DT, int DP>
 int launch_ws(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const thd::AttnParams& p,
               int grid, cudaStream_t stream) {
   auto kern = thd::attn_fwd_ws_kernel<DT, DP>;
-  const size_t smem = sizeof(thd::WsSmem<DP>) + 1024;
+  const size_t smem = one_cta_per_sm(sizeof(thd::WsSmem<DP>) + 1024);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return THD_ERR_CUDA;
   kern<<<grid, thd::kWsThreads, smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
 }
 
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t bwd_workspace_bytes(int T, int Hq, int d) {
+  return kWorkspaceBytes + align256((size_t)Hq * T * 4) + align256((size_t)T * Hq * d * 4);
+}
+
+template <typename DT, int DP>
+int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+               const thd::BwdParams& bp, int sms, cudaStream_t stream) {
+  const int small_grid = sms * 8;
+  thd::attn_bwd_pre_kernel<DT><<<small_grid, 256, 0, stream>>>(bp);
+  if (cudaGetLastError() != cudaSuccess) return THD_ERR_CUDA;
+  auto kern = thd::attn_bwd_kernel<DT, DP>;
+  const size_t smem = one_cta_per_sm(sizeof(thd::BwdSmem<DP>) + 1024);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return THD_ERR_CUDA;
+  kern<<<sms, 128, smem, stream>>>(mq, mk, mv, mdo, bp);
+  if (cudaGetLastError() != cudaSuccess) return THD_ERR_CUDA;
+  thd::attn_bwd_post_kernel<DT><<<small_grid, 256, 0, stream>>>(bp);
+  return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t thd_attn_bwd_workspace_size(int total_tokens, int num_heads_q, int head_dim) {
+  if (total_tokens < 0 || num_heads_q < 1 || head_dim < 1) return 0;
+  return bwd_workspace_bytes(total_tokens, num_heads_q, head_dim);
+}
+
+int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size, int max_seqlen,
+                 float softmax_scale, void* dq, void* dk, void* dv, int total_tokens, int num_heads_q,
+                 int num_heads_kv, int head_dim, int dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  if (batch_size < 0 || max_seqlen < 0 || total_tokens < 0) return THD_ERR_ARG;
+  if (num_heads_q < 1 || num_heads_kv < 1) return THD_ERR_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return THD_ERR_ARG;
+  if (dtype != THD_BF16 && dtype != THD_FP16) return THD_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return THD_ERR_UNSUPPORTED;
+  if (num_heads_q % num_heads_kv != 0) return THD_ERR_UNSUPPORTED;
+  const long long max_items = ((long long)total_tokens / 128 + (long long)batch_size + 1) * num_heads_kv;
+  if (max_items >= (1ll << 31)) return THD_ERR_UNSUPPORTED;
+  if ((long long)num_heads_q * head_dim * 2 >= (1ll << 31)) return THD_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return THD_OK;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return THD_ERR_ARG;
+  if (batch_size > 0 && (!cu_seqlens_q || !cu_seqlens_kv)) return THD_ERR_ARG;
+  const void* a16[] = {q, k, v, out, dout, dq, dk, dv};
+  for (const void* ptr : a16)
+    if (!aligned(ptr, 16)) return THD_ERR_ARG;
+  if (!aligned(lse, 4) || (cu_seqlens_q && !aligned(cu_seqlens_q, 4)) ||
+      (cu_seqlens_kv && !aligned(cu_seqlens_kv, 4)) ||
+      (cu_seqlens_q_padded && !aligned(cu_seqlens_q_padded, 4)) ||
+      (cu_seqlens_kv_padded && !aligned(cu_seqlens_kv_padded, 4)))
+    return THD_ERR_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < bwd_workspace_bytes(total_tokens, num_heads_q, head_dim))
+    return THD_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return THD_ERR_CUDA;
+
+  thd::BwdParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  thd::AttnParams& p = bp.a;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.pad_q = cu_seqlens_q_padded;
+  p.pad_kv = cu_seqlens_kv_padded;
+  p.causal = seq_is_causal;
+  p.out = const_cast<void*>(out);
+  p.lse = const_cast<float*>(lse);
+  p.work_counter = static_cast<unsigned long long*>(workspace);
+  p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
+  p.B = batch_size;
+  p.T = total_tokens;
+  p.Hq = num_heads_q;
+  p.Hkv = num_heads_kv;
+  p.d = head_dim;
+  p.group = num_heads_q / num_heads_kv;
+  p.scale = softmax_scale;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  bp.dout = dout;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv = dv;
+  char* wsb = static_cast<char*>(workspace);
+  bp.D = reinterpret_cast<float*>(wsb + kWorkspaceBytes);
+  bp.dacc = reinterpret_cast<float*>(wsb + kWorkspaceBytes + align256((size_t)num_heads_q * total_tokens * 4));
+
+  if (cudaMemsetAsync(workspace, 0, 16, st) != cudaSuccess) return THD_ERR_CUDA;
+  const bool bf16 = dtype == THD_BF16;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_thd_map(&mq, q, total_tokens, num_heads_q, head_dim, bf16) ||
+      !encode_thd_map(&mk, k, total_tokens, num_heads_kv, head_dim, bf16) ||
+      !encode_thd_map(&mv, v, total_tokens, num_heads_kv, head_dim, bf16) ||
+      !encode_thd_map(&mdo, dout, total_tokens, num_heads_q, head_dim, bf16))
+    return THD_ERR_CUDA;
+  if (bf16) {
+    if (head_dim == 128) return launch_bwd<__nv_bfloat16, 128>(mq, mk, mv, mdo, bp, sms, st);
+    return launch_bwd<__nv_bfloat16, 64>(mq, mk, mv, mdo, bp, sms, st);
+  }
+  if (head_dim == 128) return launch_bwd<__half, 128>(mq, mk, mv, mdo, bp, sms, st);
+  return launch_bwd<__half, 64>(mq, mk, mv, mdo, bp, sms, st);
+}
+
 
 const char* thd_status_string(int status) {
   switch (status) {

@@ -331,3 +331,10 @@ def merge_inputs(T, H, d, dtype, seed):
         lse[m] = float("-inf")
         out.permute(1, 0, 2)[m] = 0
     return out_a, lse_a, out_b, lse_b
+
+
+def grad_output(w, seed):
+    """dO for backward tests: N(0, 1) of out's shape [T, Hq, d] in w's dtype (CPU)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return torch.randn((w.total_tokens, w.num_heads_q, w.head_dim), generator=g,
+                       dtype=torch.float32).to(w.dtype)
