@@ -313,6 +313,35 @@ def run_gpu(args, ws, rank, local):
                               "effective_tflops": eff / (attn_ms * 1e-3) / 1e12, "status": status}), flush=True)
         return 0
 
+    # ---- backward on the same batch (dQ, dK, dV; the forward's out / lse as inputs) ----
+    backward = None
+    if not args.no_backward:
+        gdo = torch.Generator(device=dev).manual_seed(5)
+        dout = torch.randn(w.q.shape, generator=gdo, device=dev, dtype=torch.float32).to(w.dtype)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(vlp.load_library().thd_attn_bwd_workspace_size(w.total_tokens, w.num_heads_q,
+                                                                          w.head_dim), dtype=torch.uint8, device=dev)
+
+        def bcall():
+            vlp.thd_attn_bwd(q, k, v, out, lse, dout, cu, cu, None, None, causal, w.batch_size, S, w.softmax_scale,
+                             dq=dq, dk=dk, dv=dv, workspace=bws)
+        for _ in range(3):
+            bcall()
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        breps = 5
+        b0.record(stream)
+        for _ in range(breps):
+            bcall()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bms = b0.elapsed_time(b1) / breps
+        beff = 2.5 * eff   # five products (S, dP, dV, dK, dQ) against the forward's two
+        backward = {"ms_per_call": bms, "effective_tflops": beff / (bms * 1e-3) / 1e12,
+                    "frac_of_bf16_peak": beff / (bms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                    "launches_per_call": 3, "flops_counted": "2.5 x forward effective FLOPs"}
+        del dout, dq, dk, dv, bws
+
     # ---- the other packed batches: attention alone, same kernel, inputs drawn on the device ----
     others = {}
     for name in args.also:
@@ -436,6 +465,7 @@ def run_gpu(args, ws, rank, local):
         "e2e": {"value": ws * eff / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "other_workloads": others,
+        "backward": backward,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.result,
         "device_status_word": status,
@@ -463,6 +493,7 @@ def main():
                     help="packed batch to run (default: the long-context workload the metric is quoted on)")
     ap.add_argument("--also", nargs="*", default=["padded_gaps", "mixed_gqa", "many_short"],
                     help="other packed batches whose attention launch is timed alone (after the step)")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--attn-only", action="store_true",
                     help="run only the attention launches (warm-up + timed) and print the line; "
                          "for profiler captures")

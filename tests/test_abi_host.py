@@ -91,3 +91,34 @@ def test_binding_refuses_cpu_tensors(lib):
         vlp.thd_attn_fwd(x, x, x, cu, cu)
     with pytest.raises(TypeError):
         vlp.thd_padding_mask(cu, 1, 4)
+
+
+def test_bwd_and_merge_arguments_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    assert lib.thd_attn_bwd_workspace_size(100, 4, 128) == 256 + 1792 + 204800
+    assert lib.thd_attn_bwd_workspace_size(-1, 4, 128) == 0
+
+    def bwd(**over):
+        a = dict(ptr=16, B=1, S=8, scale=0.1, T=100, Hq=4, Hkv=2, d=128, dtype=0, ws=256,
+                 ws_bytes=lib.thd_attn_bwd_workspace_size(100, 4, 128), lse=16)
+        a.update(over)
+        x = a["ptr"]
+        return lib.thd_attn_bwd(P(x), P(x), P(x), P(x), P(a["lse"]), P(x), P(x), P(x), P(None), P(None), P(None),
+                                a["B"], a["S"], ctypes.c_float(a["scale"]), P(x), P(x), P(x), a["T"], a["Hq"],
+                                a["Hkv"], a["d"], a["dtype"], P(a["ws"]), ctypes.c_size_t(a["ws_bytes"]), P(None))
+    assert bwd(d=96) == -2 and bwd(d=40) == -2 and bwd(Hq=3) == -2 and bwd(dtype=5) == -2
+    assert bwd(B=-1) == -1 and bwd(scale=0.0) == -1 and bwd(lse=None) == -1 and bwd(ptr=24) == -1
+    assert bwd(ws=128) == -4 and bwd(ws_bytes=1024) == -4 and bwd(ws=None) == -4
+    assert bwd(T=0, ptr=None, lse=None) == 0
+
+    def merge(**over):
+        a = dict(ptr=16, lse=16, T=10, H=2, d=64, dtype=0)
+        a.update(over)
+        return lib.thd_attn_merge(P(a["ptr"]), P(a["lse"]), P(a["ptr"]), P(a["lse"]), P(a["ptr"]), P(a["lse"]),
+                                  a["T"], a["H"], a["d"], a["dtype"], P(None))
+    assert merge(d=4) == -2 and merge(d=136) == -2 and merge(dtype=3) == -2
+    assert merge(T=-1) == -1 and merge(H=0) == -1 and merge(ptr=8) == -1 and merge(lse=2) == -1
+    assert merge(ptr=None) == -1 and merge(T=0, ptr=None, lse=None) == 0
+    assert lib.thd_padding_mask_cross(P(16), P(16), -1, 4, 4, P(16), P(16), P(None)) == -1
+    assert lib.thd_padding_mask_cross(P(16), P(16), 0, 4, 4, P(None), P(None), P(None)) == 0
+    assert lib.thd_padding_mask_cross(P(None), P(16), 2, 4, 4, P(16), P(16), P(None)) == -1
