@@ -40,6 +40,7 @@ struct AttnParams {
   float* lse;              // may be null
   unsigned long long* work_counter;
   uint32_t* status;
+  int claim;               // work items taken per atomic on the counter (>= 1)
   int B, T, Hq, Hkv, d, group;
   float scale;             // softmax scale
   float scale_log2;        // softmax scale * log2(e)
@@ -108,12 +109,14 @@ __device__ __forceinline__ int kv_tiles_for(const SeqInfo& s, int q0, int rows) 
 // chunk order in its shared memory from the device metadata, so no host
 // synchronisation and no second launch are needed.
 // ----------------------------------------------------------------------------
-constexpr int kSchedChunk = 1024;
+constexpr int kSchedChunk = 512;
 constexpr int kSchedBuckets = 1024;
 
 struct SchedSmem {
   uint32_t off[kSchedBuckets];      // histogram, then running bucket offsets
   uint32_t cum[kSchedChunk + 1];    // exclusive prefix of item counts, sorted order
+  int4 span[kSchedChunk];           // decoded (q_start, q_len, kv_start, kv_len) per chunk-local sequence
+  uint8_t code[kSchedChunk];        // mask type code per chunk-local sequence
   uint16_t key[kSchedChunk];        // sort key per chunk-local sequence
   uint16_t order[kSchedChunk];      // chunk-local sequence ids, sorted
   int chunk_base;
@@ -148,6 +151,19 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
   return x;
 }
 
+// Sequence info of chunk-local sequence i, from the chunk's cache (no global loads).
+__device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i) {
+  const int4 sp = s.span[i];
+  SeqInfo si;
+  si.q_start = sp.x;
+  si.q_len = sp.y;
+  si.kv_start = sp.z;
+  si.kv_len = sp.w;
+  si.causal = s.code[i] != kMaskPadding;
+  si.shift = s.code[i] == kMaskCausalBottomRight ? sp.w - sp.y : 0;
+  return si;
+}
+
 // Load and sort the chunk of sequences starting at `base`.  One full warp.
 template <int BLOCK_M, bool kKvSide = false>
 __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
@@ -156,7 +172,11 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   for (int i = lane; i < kSchedBuckets; i += 32) s.off[i] = 0u;
   __syncwarp();
   for (int i = lane; i < n; i += 32) {
-    uint32_t k = seq_sort_key(load_seq(p, base + i));
+    const SeqInfo si = load_seq(p, base + i);
+    s.span[i] = make_int4(si.q_start, si.q_len, si.kv_start, si.kv_len);
+    const int raw = p.causal ? (int)p.causal[base + i] : kMaskPadding;
+    s.code[i] = (uint8_t)(raw == kMaskPadding ? kMaskPadding : (raw == kMaskCausalBottomRight ? raw : 1));
+    const uint32_t k = seq_sort_key(si);
     s.key[i] = (uint16_t)k;
     atomicAdd(&s.off[k], 1u);
   }
@@ -190,7 +210,7 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   uint32_t carry = 0;
   for (int j0 = 0; j0 < n; j0 += 32) {
     const int j = j0 + lane;
-    const uint32_t it = j < n ? seq_items<BLOCK_M, kKvSide>(load_seq(p, base + s.order[j]), p) : 0u;
+    const uint32_t it = j < n ? seq_items<BLOCK_M, kKvSide>(cached_seq(s, s.order[j]), p) : 0u;
     const uint32_t incl = warp_incl_scan(it);
     if (j < n) s.cum[j + 1] = carry + incl;
     carry += __shfl_sync(0xffffffffu, incl, 31);
@@ -237,7 +257,7 @@ __device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned lon
     if (s.cum[mid] <= local) lo = mid; else hi = mid;
   }
   it.b = s.chunk_base + s.order[lo];
-  it.seq = load_seq(p, it.b);
+  it.seq = cached_seq(s, s.order[lo]);
   const uint32_t r = local - s.cum[lo];
   const int len = kKvSide ? it.seq.kv_len : it.seq.q_len;
   const uint32_t nblk = (uint32_t)((len + BLOCK_M - 1) / BLOCK_M);
@@ -245,6 +265,24 @@ __device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned lon
   it.qblock = kKvSide ? (int)(r % nblk) : (int)(nblk - 1u - (r % nblk));
   it.valid = 1;
   return it;
+}
+
+// Global work counter, p.claim items per atomic (fewer round trips when items
+// are small).  Call with the whole warp; the claimed indices of one CTA increase.
+struct Claimer {
+  unsigned long long base;
+  int left;
+};
+__device__ __forceinline__ unsigned long long claim_item(Claimer& c, const AttnParams& p) {
+  if (c.left == 0) {
+    unsigned long long b = 0;
+    if ((threadIdx.x & 31) == 0) b = atomicAdd(p.work_counter, (unsigned long long)p.claim);
+    c.base = __shfl_sync(0xffffffffu, b, 0);
+    c.left = p.claim;
+  }
+  const unsigned long long w = c.base + (unsigned long long)(p.claim - c.left);
+  --c.left;
+  return w;
 }
 
 __device__ __forceinline__ void sched_init(SchedSmem& s) {

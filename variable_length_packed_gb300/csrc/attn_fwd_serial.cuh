@@ -91,11 +91,10 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t ph_load = 0, ph_mma = 0;
   volatile uint32_t* abort_flag = &sm.abort;
 
+  Claimer claimer{0ull, 0};   // used by warp 0
   for (;;) {
     if (warp == 0) {
-      unsigned long long w = 0;
-      if (lane == 0) w = atomicAdd(p.work_counter, 1ull);
-      w = __shfl_sync(0xffffffffu, w, 0);
+      const unsigned long long w = claim_item(claimer, p);
       WorkItem it = sched_decode<kTileM>(sm.sched, p, w);
       if (lane == 0) sm.item = it;
     }

@@ -33,18 +33,22 @@
 namespace thd {
 
 constexpr int kWsBlockM = 256;   // query rows per work item (two Q tiles)
-constexpr int kWsStages = 2;     // K/V ring depth
+// Ring depths: head_dim 128 fills shared memory with one Q slot (two tiles) and
+// two K/V stages; head_dim 64 has room for two Q slots (the next item's Q loads
+// while the current one computes) and four K/V stages.
+template <int DP> struct WsDepth { static constexpr int kQSlots = DP == 64 ? 2 : 1, kStages = DP == 64 ? 4 : 2; };
 constexpr int kWsThreads = 320;  // 10 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int DP>
 struct WsSmem {
   static constexpr int kTileBytes = kTileM * DP * 2;
-  alignas(1024) uint8_t q[2][kTileBytes];
-  alignas(1024) uint8_t k[kWsStages][kTileBytes];
-  alignas(1024) uint8_t v[kWsStages][kTileBytes];
-  uint64_t q_full, q_empty;
-  uint64_t k_full[kWsStages], v_full[kWsStages], k_empty[kWsStages], v_empty[kWsStages];
+  static constexpr int kQSlots = WsDepth<DP>::kQSlots, kStages = WsDepth<DP>::kStages;
+  alignas(1024) uint8_t q[kQSlots][2][kTileBytes];
+  alignas(1024) uint8_t k[kStages][kTileBytes];
+  alignas(1024) uint8_t v[kStages][kTileBytes];
+  uint64_t q_full[kQSlots], q_empty[kQSlots];
+  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_lo[2], p_hi[2], o_full[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
@@ -123,13 +127,13 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
                             const CUtensorMap* tm_v, volatile uint32_t* abort_flag) {
   constexpr uint32_t kTileBytes = WsSmem<DP>::kTileBytes;
   constexpr int kPanels = DP / 64;
+  constexpr int kQSlots = WsSmem<DP>::kQSlots, kWsStages = WsSmem<DP>::kStages;
   const int lane = threadIdx.x & 31;
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0;
   bool ok = true;
+  Claimer claimer{0ull, 0};
   for (;;) {
-    unsigned long long w = 0;
-    if (lane == 0) w = atomicAdd(p.work_counter, 1ull);
-    w = __shfl_sync(0xffffffffu, w, 0);
+    const unsigned long long w = claim_item(claimer, p);
     WorkItem it = sched_decode<kWsBlockM>(sm.sched, p, w);
     const int slot = it_cnt & 1;
     if (lane == 0) {
@@ -142,30 +146,31 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
     ++it_cnt;
     if (!it.valid || !ok) break;
     const ItemGeom g = item_geom(it, p);
-    if (g.n_all == 0) continue;
-    if (lane == 0) {
+    if (lane == 0 && g.n_all > 0) {
       const SeqInfo& s = it.seq;
-      if (q_cnt >= 1) ok = WS_WAIT(&sm.q_empty, (q_cnt - 1) & 1);
+      const int qs = q_cnt % kQSlots;
+      if (q_cnt >= (uint32_t)kQSlots) ok = WS_WAIT(&sm.q_empty[qs], ((q_cnt / kQSlots) - 1) & 1);
       if (ok) {
         const int ntiles = g.rows[1] > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(&sm.q_full, ntiles * kTileBytes);
+        mbar_arrive_expect_tx(&sm.q_full[qs], ntiles * kTileBytes);
         for (int t = 0; t < ntiles; ++t)
 #pragma unroll
           for (int pn = 0; pn < kPanels; ++pn)
-            tma_load_2d(sm.q[t] + pn * 16384, tm_q, &sm.q_full, it.h * p.d + pn * 64, s.q_start + g.q0 + t * kTileM);
+            tma_load_2d(sm.q[qs][t] + pn * 16384, tm_q, &sm.q_full[qs], it.h * p.d + pn * 64,
+                        s.q_start + g.q0 + t * kTileM);
         ++q_cnt;
       }
       for (int j = 0; ok && j < g.n_all; ++j) {
         const int st = kv_cnt % kWsStages;
         const uint32_t reuse = ((kv_cnt / kWsStages) - 1) & 1;
-        if (kv_cnt >= kWsStages) ok = WS_WAIT(&sm.k_empty[st], reuse);
+        if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.k_empty[st], reuse);
         if (!ok) break;
         const int row = s.kv_start + j * kBlockN;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
           tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], g.kvh * p.d + pn * 64, row);
-        if (kv_cnt >= kWsStages) ok = WS_WAIT(&sm.v_empty[st], reuse);
+        if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.v_empty[st], reuse);
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
 #pragma unroll
@@ -179,8 +184,9 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   }
   // copies still in flight land before the CTA can exit
   if (lane == 0) {
-    if (q_cnt > 0) drain_wait(&sm.q_full, (q_cnt - 1) & 1);
-    for (uint32_t c = (kv_cnt > kWsStages ? kv_cnt - kWsStages : 0); c < kv_cnt; ++c) {
+    for (uint32_t c = (q_cnt > (uint32_t)kQSlots ? q_cnt - kQSlots : 0); c < q_cnt; ++c)
+      drain_wait(&sm.q_full[c % kQSlots], (c / kQSlots) & 1);
+    for (uint32_t c = (kv_cnt > (uint32_t)kWsStages ? kv_cnt - kWsStages : 0); c < kv_cnt; ++c) {
       drain_wait(&sm.k_full[c % kWsStages], (c / kWsStages) & 1);
       drain_wait(&sm.v_full[c % kWsStages], (c / kWsStages) & 1);
     }
@@ -199,8 +205,9 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 256 + DP};
   // low descriptor words; consecutive tiles / stages are kTileBytes apart
+  constexpr int kQSlots = WsSmem<DP>::kQSlots, kWsStages = WsSmem<DP>::kStages;
   constexpr uint32_t kStep = WsSmem<DP>::kTileBytes >> 4;
-  const uint32_t q_lo0 = smem_desc_sw128_lo(smem_u32(sm.q[0]), 16);
+  const uint32_t q_lo00 = smem_desc_sw128_lo(smem_u32(sm.q[0][0]), 16);
   const uint32_t k_lo0 = smem_desc_sw128_lo(smem_u32(sm.k[0]), 16);
   const uint32_t v_lo0 = smem_desc_sw128_lo(smem_u32(sm.v[0]), 16384);
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, p_cnt[2] = {0, 0};
@@ -214,8 +221,10 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     const ItemGeom g = item_geom(it, p);
     const int n = g.n_all;
     if (n == 0) continue;
-    if (!WS_WAIT(&sm.q_full, q_cnt & 1)) break;
+    const int qs = q_cnt % kQSlots;
+    if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
     ++q_cnt;
+    const uint32_t q_lo0 = q_lo00 + qs * 2 * kStep;   // this slot's tile 0
     if (!WS_WAIT(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
     tc_fence_after();
     {
@@ -228,7 +237,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         }
       }
       umma_commit(&sm.k_empty[kv_cnt % kWsStages]);
-      if (n == 1) umma_commit(&sm.q_empty);
+      if (n == 1) umma_commit(&sm.q_empty[qs]);
     }
     bool ok = true;
     for (int j = 0; j < n && ok; ++j) {
@@ -256,7 +265,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         }
       }
       if (j + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
-      if (j == n - 2) umma_commit(&sm.q_empty);        // last S MMAs of the item issued
+      if (j == n - 2) umma_commit(&sm.q_empty[qs]);    // last S MMAs of the item issued
       umma_commit(&sm.v_empty[st]);
     }
     kv_cnt += n;
@@ -441,9 +450,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
-    for (int s = 0; s < kWsStages; ++s) {
+    for (int s = 0; s < WsSmem<DP>::kQSlots; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    for (int s = 0; s < WsSmem<DP>::kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);

@@ -53,6 +53,19 @@ int num_sms_of_current_device() {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Work items claimed per atomic on the scheduler's counter.  With short
+// sequences (the max_seqlen hint) an item is a few microseconds of work and the
+// atomic's round trip would dominate; long items take one at a time so the
+// longest-first order still balances the tail.  Any value is correct.
+int claim_for(int max_seqlen, long long min_items, int ctas) {
+  if (max_seqlen <= 0) return 1;
+  int c = 2048 / max_seqlen;
+  // every CTA should still get several claims: batch * heads is a lower bound on the items
+  const long long per_cta = min_items / (8ll * (ctas > 0 ? ctas : 1));
+  if (c > per_cta) c = (int)per_cta;
+  return c < 1 ? 1 : (c > 8 ? 8 : c);
+}
+
 // 2-D view [rows, heads * d] of a THD tensor, box = 128 rows x 64 columns,
 // 128-byte swizzle (the layout the UMMA shared-memory descriptors expect).
 bool encode_thd_map(CUtensorMap* map, const void* base, int rows, int heads, int d, bool bf16) {
@@ -176,6 +189,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
   p.lse = const_cast<float*>(lse);
   p.work_counter = static_cast<unsigned long long*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
+  p.claim = claim_for(max_seqlen, (long long)batch_size * num_heads_kv, sms);
   p.B = batch_size;
   p.T = total_tokens;
   p.Hq = num_heads_q;
@@ -309,6 +323,7 @@ int thd_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_
   p.lse = lse;
   p.work_counter = static_cast<unsigned long long*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
+  p.claim = claim_for(max_seqlen, (long long)batch_size * num_heads_q, sms);
   p.B = batch_size;
   p.T = total_tokens;
   p.Hq = num_heads_q;
