@@ -38,9 +38,12 @@ import workloads  # noqa: E402
 METRIC = "THD attn fwd effective TFLOP/s and % of GB300 dense BF16 peak; mask GB/s"
 WORKLOAD = "long_context"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["variable_length_packed_gb300/csrc/" + f for f in
-                  ("ptx.cuh", "attn_common.cuh", "attn_fwd_serial.cuh", "attn_fwd_ws.cuh", "thd_attn.cu",
-                   "padding_mask.cu")]
+# Sources of each kernel whose profiler counters are recorded under profiles/ (a counter
+# record is used only while these files are unchanged).
+KERNEL_SOURCES = {
+    "attn_fwd": ["variable_length_packed_gb300/csrc/" + f for f in ("ptx.cuh", "attn_common.cuh", "attn_fwd_ws.cuh")],
+    "padding_mask": ["variable_length_packed_gb300/csrc/padding_mask.cu"],
+}
 
 
 def effective_flops(w):
@@ -65,9 +68,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_sources_sha():
+def kernel_sources_sha(kind):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         path = os.path.join(ROOT, rel)
         if os.path.exists(path):
             with open(path, "rb") as f:
@@ -86,7 +89,7 @@ def recorded_traffic(kind):
             if ":" in line and not line.startswith("#"):
                 k, _, v = line.partition(":")
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources_sha256") != kernel_sources_sha():
+    if vals.get("kernel_sources_sha256") != kernel_sources_sha(kind):
         return None
     try:
         return float(vals["dram_bytes_per_launch_full_workload"])
