@@ -14,8 +14,8 @@ import torch
 import oracle
 import workloads
 from conftest import read_golden
-from thd_testutil import (boundary_rows, check_pad_rows, compare_full, compare_sampled, run_gpu,
-                          to_device, valid_rows)
+from thd_testutil import (LSE_ATOL, OUT_ATOL, boundary_rows, check_pad_rows, compare_full, compare_sampled,
+                          run_gpu, to_device, valid_rows)
 
 pytestmark = pytest.mark.gpu
 vlp = pytest.importorskip("variable_length_packed_gb300")
@@ -120,6 +120,62 @@ def test_head_dims_and_tile_boundaries(d, dtype):
                                heads_q=4, heads_kv=2, head_dim=d, dtype=dtype, seed=d)
     out, lse = run_gpu(w)
     compare_full(w, out, lse)
+
+
+@pytest.mark.parametrize("d,dtype", [(64, torch.float16), (128, torch.bfloat16)])
+def test_paired_short_tiles_across_chunks(d, dtype):
+    """Sequences of at most 128 rows run as independent (sequence, head) tiles two per unit,
+    longer ones as 256-row blocks: 700 sequences (two scheduler chunks of 512), three query
+    heads on one KV head (odd tile counts per chunk), zero-length sequences, lengths 128 / 129."""
+    rng = np.random.default_rng(70 + d)
+    B = 700
+    lens = rng.integers(1, 129, size=B)
+    lens[rng.choice(B, 60, replace=False)] = rng.integers(129, 400, size=60)
+    lens[rng.choice(B, 20, replace=False)] = 0
+    lens[:5] = [128, 129, 1, 0, 128]
+    causal = rng.random(B) < 0.5
+    gaps = rng.integers(0, 9, size=B)
+    w = workloads.from_lengths("paired", lens, causal, gaps_before=gaps, trailing=5, heads_q=3, heads_kv=1,
+                               head_dim=d, dtype=dtype, seed=d, with_padded=True)
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws)
+    assert status_word(ws) == 0
+    compare_full(w, out, lse)
+
+
+@pytest.mark.parametrize("d,dtype", [(64, torch.bfloat16), (128, torch.float16)])
+def test_paired_short_cross_sequences(d, dtype):
+    """Short sequences with separate query / key spans and all three mask types (bottom-right
+    with fewer keys than queries leaves leading rows without keys; empty key spans)."""
+    rng = np.random.default_rng(90 + d)
+    B = 41
+    lq = rng.integers(1, 129, size=B)
+    lkv = rng.integers(0, 129, size=B)
+    lkv[:3] = [0, 128, 5]
+    lq[:3] = [9, 128, 100]
+    codes = rng.integers(0, 3, size=B).astype(np.uint8)
+    q_starts = np.concatenate([[0], np.cumsum(lq + 3)[:-1]]).astype(np.int32)
+    kv_starts = (np.concatenate([[0], np.cumsum(lkv + 1)[:-1]]) + 7).astype(np.int32)
+    T = int(max(q_starts[-1] + lq[-1], kv_starts[-1] + lkv[-1]) + 2)
+    w = workloads.from_lengths("cross", [T], [0], heads_q=2, heads_kv=2, head_dim=d, dtype=dtype, seed=d)
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    ws = workspace()
+    out, lse = vlp.thd_attn_fwd(w.q.cuda(), w.k.cuda(), w.v.cuda(), dev(cu_q), dev(cu_k), dev(q_starts),
+                                dev(kv_starts), dev(codes), B, 128, w.softmax_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert status_word(ws) == 0
+    ref, ref_lse = oracle.thd_attention_fwd_general(w.q, w.k, w.v, cu_q, cu_k, q_starts, kv_starts, codes, B,
+                                                    w.softmax_scale)
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    seen = np.isfinite(ref_lse)
+    assert np.abs(o - ref).max() <= OUT_ATOL[dtype]
+    assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
+    assert np.all(np.isneginf(l[~seen]))
+    assert np.all(o[~seen.any(axis=0)] == 0.0)
+    assert (~seen).sum() > 0
 
 
 @pytest.mark.parametrize("group", [1, 2, 4, 8])

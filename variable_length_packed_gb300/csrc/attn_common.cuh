@@ -121,14 +121,34 @@ struct SchedSmem {
   uint16_t order[kSchedChunk];      // chunk-local sequence ids, sorted
   int chunk_base;
   int chunk_n;
+  int n_short;                      // kPairs: short sequences, at sorted positions [n_long, n_long + n_short)
+  int n_long;                       // kPairs: long sequences, at sorted positions [0, n_long)
   unsigned long long item_base;
   unsigned long long item_end;
 };
 
+// A short sequence fits one Q tile and one KV tile.  With kPairs (the
+// warp-specialised forward), short sequences are not split into BLOCK_M items:
+// their (sequence, head) tiles are taken two at a time, each with its own K/V.
+__device__ __forceinline__ bool seq_is_short(const SeqInfo& s) {
+  return s.q_len > 0 && s.q_len <= kTileM && s.kv_len <= kBlockN;
+}
+
+// Sort key (descending order = processing order).  Plain: KV tiles, full
+// context before causal at equal length.  kPairs: long sequences (keys >= 3)
+// first in the same order, then short sequences (2 full context, 1 causal),
+// then sequences without query rows (0), so short sequences form a suffix.
+template <bool kPairs = false>
 __device__ __forceinline__ uint32_t seq_sort_key(const SeqInfo& s) {
   int nkv = (s.kv_len + kBlockN - 1) / kBlockN;
-  nkv = nkv > 511 ? 511 : nkv;
-  return (uint32_t)(nkv * 2 + (s.causal ? 0 : 1));
+  if (!kPairs) {
+    nkv = nkv > 511 ? 511 : nkv;
+    return (uint32_t)(nkv * 2 + (s.causal ? 0 : 1));
+  }
+  if (s.q_len <= 0) return 0u;
+  if (seq_is_short(s)) return s.causal ? 1u : 2u;
+  nkv = nkv > 509 ? 509 : nkv;
+  return (uint32_t)(3 + nkv * 2 + (s.causal ? 0 : 1));
 }
 
 // Items of one sequence: blocks of BLOCK rows of the query sequence times the
@@ -165,7 +185,7 @@ __device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i) {
 }
 
 // Load and sort the chunk of sequences starting at `base`.  One full warp.
-template <int BLOCK_M, bool kKvSide = false>
+template <int BLOCK_M, bool kKvSide = false, bool kPairs = false>
 __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   const int lane = threadIdx.x & 31;
   const int n = min(kSchedChunk, p.B - base);
@@ -176,11 +196,15 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
     s.span[i] = make_int4(si.q_start, si.q_len, si.kv_start, si.kv_len);
     const int raw = p.causal ? (int)p.causal[base + i] : kMaskPadding;
     s.code[i] = (uint8_t)(raw == kMaskPadding ? kMaskPadding : (raw == kMaskCausalBottomRight ? raw : 1));
-    const uint32_t k = seq_sort_key(si);
+    const uint32_t k = seq_sort_key<kPairs>(si);
     s.key[i] = (uint16_t)k;
     atomicAdd(&s.off[k], 1u);
   }
   __syncwarp();
+  if (kPairs && lane == 0) {
+    s.n_short = (int)(s.off[1] + s.off[2]);
+    s.n_long = n - s.n_short - (int)s.off[0];
+  }
   // exclusive offsets, keys in descending order; lane l owns 32 consecutive keys
   uint32_t sum = 0;
   for (int t = 0; t < 32; ++t) sum += s.off[kSchedBuckets - 1 - (lane * 32 + t)];
@@ -210,7 +234,11 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   uint32_t carry = 0;
   for (int j0 = 0; j0 < n; j0 += 32) {
     const int j = j0 + lane;
-    const uint32_t it = j < n ? seq_items<BLOCK_M, kKvSide>(cached_seq(s, s.order[j]), p) : 0u;
+    uint32_t it = 0u;
+    if (j < n) {
+      const SeqInfo sj = cached_seq(s, s.order[j]);
+      it = (kPairs && seq_is_short(sj)) ? 0u : seq_items<BLOCK_M, kKvSide>(sj, p);
+    }
     const uint32_t incl = warp_incl_scan(it);
     if (j < n) s.cum[j + 1] = carry + incl;
     carry += __shfl_sync(0xffffffffu, incl, 31);
@@ -235,27 +263,51 @@ struct WorkItem {
 // blocks, heaviest (last) first; backward (kKvSide): key/value blocks and
 // heads, lowest block first (under causal masking the first keys are seen by
 // the most queries).
-template <int BLOCK_M, bool kKvSide = false>
-__device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
-  WorkItem it;
-  it.valid = 0;
+// Items (units, with kPairs) of the loaded chunk: the long sequences' items,
+// then the short sequences' (sequence, head) tiles two per unit.
+template <bool kPairs>
+__device__ __forceinline__ unsigned long long chunk_items(const SchedSmem& s, const AttnParams& p) {
+  unsigned long long n = s.cum[s.chunk_n];
+  if (kPairs) n += ((unsigned long long)s.n_short * (unsigned long long)p.Hq + 1ull) / 2ull;
+  return n;
+}
+
+// Loads later chunks until the one holding global item w; false when w is
+// past the last item.  One full warp.
+template <int BLOCK_M, bool kKvSide = false, bool kPairs = false>
+__device__ bool sched_seek(SchedSmem& s, const AttnParams& p, unsigned long long w) {
   while (w >= s.item_end) {
     const int next = s.chunk_base + s.chunk_n;
-    if (next >= p.B) return it;
+    if (next >= p.B) return false;
     const unsigned long long base_items = s.item_end;
-    sched_load_chunk<BLOCK_M, kKvSide>(s, p, next);
+    sched_load_chunk<BLOCK_M, kKvSide, kPairs>(s, p, next);
     if ((threadIdx.x & 31) == 0) {
       s.item_base = base_items;
-      s.item_end = base_items + s.cum[s.chunk_n];
+      s.item_end = base_items + chunk_items<kPairs>(s, p);
     }
     __syncwarp();
   }
-  const uint32_t local = (uint32_t)(w - s.item_base);
+  return true;
+}
+
+// Sorted position of the sequence holding chunk-local item `local` (which must
+// be below cum[chunk_n]): the last position whose prefix does not exceed it.
+__device__ __forceinline__ int sched_find(const SchedSmem& s, uint32_t local) {
   int lo = 0, hi = s.chunk_n;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s.cum[mid] <= local) lo = mid; else hi = mid;
   }
+  return lo;
+}
+
+template <int BLOCK_M, bool kKvSide = false>
+__device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
+  WorkItem it;
+  it.valid = 0;
+  if (!sched_seek<BLOCK_M, kKvSide>(s, p, w)) return it;
+  const uint32_t local = (uint32_t)(w - s.item_base);
+  const int lo = sched_find(s, local);
   it.b = s.chunk_base + s.order[lo];
   it.seq = cached_seq(s, s.order[lo]);
   const uint32_t r = local - s.cum[lo];
@@ -288,6 +340,8 @@ __device__ __forceinline__ unsigned long long claim_item(Claimer& c, const AttnP
 __device__ __forceinline__ void sched_init(SchedSmem& s) {
   s.chunk_base = 0;
   s.chunk_n = 0;
+  s.n_short = 0;
+  s.n_long = 0;
   s.item_base = 0;
   s.item_end = 0;
 }

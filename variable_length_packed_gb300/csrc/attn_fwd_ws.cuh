@@ -25,6 +25,13 @@
 // MMAs.  K and V stages are released separately: a K stage once both tiles'
 // S MMAs on it are done, a V stage once both P V MMAs are done.
 //
+// Short sequences (at most 128 query rows and 128 keys) are not blocked by
+// 256 rows: their (sequence, head) tiles are paired, two independent tiles per
+// work unit, each with its own K/V tile, and the MMA warp issues the next
+// unit's S_t right after this unit's P_t V (S_0' after P_0 V, S_1' after P_1
+// V), so the two softmax warpgroups alternate across units the way they
+// alternate across KV tiles of a long sequence.
+//
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; P_i
 // occupies the first 64 columns of S_i (two 16-bit values per column).
 #pragma once
@@ -40,6 +47,24 @@ template <int DP> struct WsDepth { static constexpr int kQSlots = DP == 64 ? 2 :
 constexpr int kWsThreads = 320;  // 10 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
+// One 128-row Q tile of a work unit.
+struct WsTile {
+  SeqInfo seq;   // the tile's sequence
+  int h;         // query head
+  int q0;        // sequence position of the tile's first query row
+  int n;         // KV tiles the tile visits (0: no row sees a key)
+};
+
+// Work unit: one block of 256 query rows of a long sequence (two tiles sharing
+// every K/V tile, `paired` = 0), or two independent short (sequence, head)
+// tiles, each with its own single K/V tile (`paired` = 1).
+struct WsUnit {
+  int valid;
+  int paired;
+  int n_all;     // K/V tiles loaded for the unit: max(n) shared, n0 + n1 paired
+  WsTile t[2];
+};
+
 template <int DP>
 struct WsSmem {
   static constexpr int kTileBytes = kTileM * DP * 2;
@@ -54,29 +79,61 @@ struct WsSmem {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
-  WorkItem items[2];
+  WsUnit items[2];
   SchedSmem sched;
 };
 
-struct ItemGeom {
-  int q0;          // first query position of the block
-  int rows[2];     // valid rows of each Q tile
-  int n[2];        // KV tiles each Q tile visits
-  int n_all;       // KV tiles loaded for the item
-  int kvh;         // key/value head
-};
-
-__device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const AttnParams& p) {
-  ItemGeom g;
-  const SeqInfo& s = it.seq;
-  g.q0 = it.qblock * kWsBlockM;
-  g.rows[0] = min(kTileM, s.q_len - g.q0);
-  g.rows[1] = max(0, min(kTileM, s.q_len - g.q0 - kTileM));
-  g.n[0] = g.rows[0] > 0 ? kv_tiles_for(s, g.q0, kTileM) : 0;
-  g.n[1] = g.rows[1] > 0 ? kv_tiles_for(s, g.q0 + kTileM, kTileM) : 0;
-  g.n_all = max(g.n[0], g.n[1]);
-  g.kvh = it.h / p.group;
-  return g;
+// Maps global unit index w to its work unit (one full warp; w never decreases
+// within a CTA).  Units of a chunk: the long sequences' 256-row blocks in the
+// scheduler's order, then the short sequences' (sequence, head) tiles, heads
+// innermost, two per unit.
+__device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
+  WsUnit u;
+  u.valid = 0;
+  u.paired = 0;
+  u.n_all = 0;
+  if (!sched_seek<kWsBlockM, false, true>(s, p, w)) return u;
+  u.valid = 1;
+  const uint32_t local = (uint32_t)(w - s.item_base);
+  const uint32_t n_long_items = s.cum[s.chunk_n];
+  if (local < n_long_items) {
+    const int pos = sched_find(s, local);
+    const SeqInfo seq = cached_seq(s, s.order[pos]);
+    const uint32_t r = local - s.cum[pos];
+    const uint32_t nblk = (uint32_t)((seq.q_len + kWsBlockM - 1) / kWsBlockM);
+    const int h = (int)(r / nblk);
+    const int qb = (int)(nblk - 1u - r % nblk);   // heaviest (last) block first
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      u.t[t].seq = seq;
+      u.t[t].h = h;
+      u.t[t].q0 = qb * kWsBlockM + t * kTileM;
+      u.t[t].n = seq.q_len > u.t[t].q0 ? kv_tiles_for(seq, u.t[t].q0, kTileM) : 0;
+    }
+    u.n_all = max(u.t[0].n, u.t[1].n);
+  } else {
+    u.paired = 1;
+    const uint32_t total = (uint32_t)s.n_short * (uint32_t)p.Hq;
+    const uint32_t i0 = 2u * (local - n_long_items);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t idx = i0 + t;
+      WsTile& tt = u.t[t];
+      if (idx < total) {
+        tt.seq = cached_seq(s, s.order[s.n_long + (int)(idx / (uint32_t)p.Hq)]);
+        tt.h = (int)(idx % (uint32_t)p.Hq);
+        tt.q0 = 0;
+        tt.n = kv_tiles_for(tt.seq, 0, kTileM);
+      } else {   // odd count: no second tile
+        tt.seq = SeqInfo{0, 0, 0, 0, 0, 0};
+        tt.h = 0;
+        tt.q0 = 0;
+        tt.n = 0;
+      }
+    }
+    u.n_all = u.t[0].n + u.t[1].n;
+  }
+  return u;
 }
 
 // S = Q K^T over head_dim DP: DP/16 K steps of 16 elements (32 bytes inside a
@@ -134,48 +191,52 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   Claimer claimer{0ull, 0};
   for (;;) {
     const unsigned long long w = claim_item(claimer, p);
-    WorkItem it = sched_decode<kWsBlockM>(sm.sched, p, w);
+    WsUnit u = ws_decode(sm.sched, p, w);
     const int slot = it_cnt & 1;
     if (lane == 0) {
       if (it_cnt >= 2) ok = WS_WAIT(&sm.item_empty[slot], ((it_cnt >> 1) - 1) & 1);
-      if (!ok) it.valid = 0;
-      sm.items[slot] = it;
+      if (!ok) u.valid = 0;
+      sm.items[slot] = u;
       mbar_arrive(&sm.item_full[slot]);
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     ++it_cnt;
-    if (!it.valid || !ok) break;
-    const ItemGeom g = item_geom(it, p);
-    if (lane == 0 && g.n_all > 0) {
-      const SeqInfo& s = it.seq;
+    if (!u.valid || !ok) break;
+    if (lane == 0 && u.n_all > 0) {
       const int qs = q_cnt % kQSlots;
       if (q_cnt >= (uint32_t)kQSlots) ok = WS_WAIT(&sm.q_empty[qs], ((q_cnt / kQSlots) - 1) & 1);
       if (ok) {
-        const int ntiles = g.rows[1] > 0 ? 2 : 1;
+        const int ntiles = (u.t[0].n > 0 ? 1 : 0) + (u.t[1].n > 0 ? 1 : 0);
         mbar_arrive_expect_tx(&sm.q_full[qs], ntiles * kTileBytes);
-        for (int t = 0; t < ntiles; ++t)
+        for (int t = 0; t < 2; ++t) {
+          if (u.t[t].n == 0) continue;   // no S MMA reads this tile
 #pragma unroll
           for (int pn = 0; pn < kPanels; ++pn)
-            tma_load_2d(sm.q[qs][t] + pn * 16384, tm_q, &sm.q_full[qs], it.h * p.d + pn * 64,
-                        s.q_start + g.q0 + t * kTileM);
+            tma_load_2d(sm.q[qs][t] + pn * 16384, tm_q, &sm.q_full[qs], u.t[t].h * p.d + pn * 64,
+                        u.t[t].seq.q_start + u.t[t].q0);
+        }
         ++q_cnt;
       }
-      for (int j = 0; ok && j < g.n_all; ++j) {
+      // K/V tiles in the order the MMA warp consumes them: KV tiles 0.. of the
+      // sequence (shared), or tile 0's then tile 1's own tile (paired)
+      for (int li = 0; ok && li < u.n_all; ++li) {
+        const int tsel = (u.paired && !(li == 0 && u.t[0].n > 0)) ? 1 : 0;
+        const int row = u.t[tsel].seq.kv_start + (u.paired ? 0 : li * kBlockN);
+        const int kvh = u.t[tsel].h / p.group;
         const int st = kv_cnt % kWsStages;
         const uint32_t reuse = ((kv_cnt / kWsStages) - 1) & 1;
         if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.k_empty[st], reuse);
         if (!ok) break;
-        const int row = s.kv_start + j * kBlockN;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
-          tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], g.kvh * p.d + pn * 64, row);
+          tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], kvh * p.d + pn * 64, row);
         if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.v_empty[st], reuse);
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
-          tma_load_2d(sm.v[st] + pn * 16384, tm_v, &sm.v_full[st], g.kvh * p.d + pn * 64, row);
+          tma_load_2d(sm.v[st] + pn * 16384, tm_v, &sm.v_full[st], kvh * p.d + pn * 64, row);
         ++kv_cnt;
       }
     }
@@ -211,65 +272,145 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   const uint32_t k_lo0 = smem_desc_sw128_lo(smem_u32(sm.k[0]), 16);
   const uint32_t v_lo0 = smem_desc_sw128_lo(smem_u32(sm.v[0]), 16384);
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, p_cnt[2] = {0, 0};
-  for (;;) {
+
+  auto fetch = [&](WsUnit& x) -> bool {
     const int slot = it_cnt & 1;
-    if (!WS_WAIT(&sm.item_full[slot], (it_cnt >> 1) & 1)) break;
-    const WorkItem it = sm.items[slot];
+    if (!WS_WAIT(&sm.item_full[slot], (it_cnt >> 1) & 1)) return false;
+    x = sm.items[slot];
     mbar_arrive(&sm.item_empty[slot]);
     ++it_cnt;
-    if (!it.valid) break;
-    const ItemGeom g = item_geom(it, p);
-    const int n = g.n_all;
-    if (n == 0) continue;
-    const int qs = q_cnt % kQSlots;
-    if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
-    ++q_cnt;
-    const uint32_t q_lo0 = q_lo00 + qs * 2 * kStep;   // this slot's tile 0
-    if (!WS_WAIT(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
+    return true;
+  };
+  // Paired unit: S_t = Q_t K_t^T on tile t's own K stage (kv_base: the unit's
+  // first K/V load); the K stage is released once the MMA completes.
+  auto pair_s = [&](const WsUnit& x, int t, uint32_t q_lo0, uint32_t kv_base) -> bool {
+    const uint32_t c = kv_base + ((t == 1 && x.t[0].n > 0) ? 1u : 0u);
+    const int st = c % kWsStages;
+    if (!WS_WAIT(&sm.k_full[st], (c / kWsStages) & 1)) return false;
     tc_fence_after();
-    {
-      const uint32_t ks = k_lo0 + (kv_cnt % kWsStages) * kStep;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (g.n[t] > 0) {
-          issue_qk<DP>(tS[t], q_lo0 + t * kStep, ks, idesc_qk);
-          umma_commit(&sm.s_full[t]);
-        }
-      }
-      umma_commit(&sm.k_empty[kv_cnt % kWsStages]);
-      if (n == 1) umma_commit(&sm.q_empty[qs]);
+    issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + st * kStep, idesc_qk);
+    umma_commit(&sm.s_full[t]);
+    umma_commit(&sm.k_empty[st]);
+    return true;
+  };
+
+  WsUnit u;
+  bool s_issued = false;   // S MMAs of the paired unit u already issued (ahead of u)
+  if (!fetch(u)) u.valid = 0;
+  while (u.valid) {
+    if (u.n_all == 0) {
+      if (!fetch(u)) break;
+      s_issued = false;
+      continue;
     }
-    bool ok = true;
-    for (int j = 0; j < n && ok; ++j) {
-      const uint32_t c = kv_cnt + j, cn = c + 1;
-      const int st = c % kWsStages, stn = cn % kWsStages;
-      if (!WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
-      const uint32_t vs = v_lo0 + st * kStep;
+    if (!u.paired) {
+      // ---- one long-sequence block: both tiles share every K/V tile ----
+      const int n = u.n_all;
+      const int qs = q_cnt % kQSlots;
+      if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
+      ++q_cnt;
+      const uint32_t q_lo0 = q_lo00 + qs * 2 * kStep;   // this slot's tile 0
+      if (!WS_WAIT(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
+      tc_fence_after();
+      {
+        const uint32_t ks = k_lo0 + (kv_cnt % kWsStages) * kStep;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (j >= g.n[t]) continue;
+        for (int t = 0; t < 2; ++t) {
+          if (u.t[t].n > 0) {
+            issue_qk<DP>(tS[t], q_lo0 + t * kStep, ks, idesc_qk);
+            umma_commit(&sm.s_full[t]);
+          }
+        }
+        umma_commit(&sm.k_empty[kv_cnt % kWsStages]);
+        if (n == 1) umma_commit(&sm.q_empty[qs]);
+      }
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const uint32_t c = kv_cnt + j, cn = c + 1;
+        const int st = c % kWsStages, stn = cn % kWsStages;
+        if (!WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
+        const uint32_t vs = v_lo0 + st * kStep;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j >= u.t[t].n) continue;
+          const uint32_t par = p_cnt[t] & 1;
+          ++p_cnt[t];
+          if (!WS_WAIT(&sm.p_lo[t], par)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, j > 0);
+          if (!WS_WAIT(&sm.p_hi[t], par)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
+          umma_commit(&sm.o_full[t]);
+          if (j + 1 < u.t[t].n) {
+            if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + stn * kStep, idesc_qk);
+            umma_commit(&sm.s_full[t]);
+          }
+        }
+        if (j + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
+        if (j == n - 2) umma_commit(&sm.q_empty[qs]);    // last S MMAs of the item issued
+        umma_commit(&sm.v_empty[st]);
+      }
+      kv_cnt += n;
+      if (!ok) break;
+      if (!fetch(u)) break;
+      s_issued = false;
+      continue;
+    }
+
+    // ---- paired unit: two independent tiles, one K/V tile each ----
+    bool ok = true;
+    if (!s_issued) {
+      const int qs = q_cnt % kQSlots;
+      if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
+      ++q_cnt;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (ok && u.t[t].n > 0) ok = pair_s(u, t, q_lo00 + qs * 2 * kStep, kv_cnt);
+      if (!ok) break;
+      umma_commit(&sm.q_empty[qs]);
+    }
+    // the next unit, if paired, gets its S_t issued right after this unit's P_t V
+    WsUnit nx;
+    if (!fetch(nx)) break;
+    const bool ahead = nx.valid && nx.paired && nx.n_all > 0;
+    const uint32_t kv_next = kv_cnt + u.n_all;
+    int qs_nx = 0;
+    if (ahead) {
+      qs_nx = q_cnt % kQSlots;
+      if (!WS_WAIT(&sm.q_full[qs_nx], (q_cnt / kQSlots) & 1)) break;
+      ++q_cnt;
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (ok && u.t[t].n > 0) {
+        const uint32_t c = kv_cnt + ((t == 1 && u.t[0].n > 0) ? 1u : 0u);
+        const int st = c % kWsStages;
+        const uint32_t vs = v_lo0 + st * kStep;
         const uint32_t par = p_cnt[t] & 1;
         ++p_cnt[t];
-        if (!WS_WAIT(&sm.p_lo[t], par)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, j > 0);
-        if (!WS_WAIT(&sm.p_hi[t], par)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
-        umma_commit(&sm.o_full[t]);
-        if (j + 1 < g.n[t]) {
-          if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
+        ok = WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1) && WS_WAIT(&sm.p_lo[t], par);
+        if (ok) {
           tc_fence_after();
-          issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + stn * kStep, idesc_qk);
-          umma_commit(&sm.s_full[t]);
+          issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, false);
+          ok = WS_WAIT(&sm.p_hi[t], par);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
+          umma_commit(&sm.o_full[t]);
+          umma_commit(&sm.v_empty[st]);
         }
       }
-      if (j + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
-      if (j == n - 2) umma_commit(&sm.q_empty[qs]);    // last S MMAs of the item issued
-      umma_commit(&sm.v_empty[st]);
+      if (ok && ahead && nx.t[t].n > 0) ok = pair_s(nx, t, q_lo00 + qs_nx * 2 * kStep, kv_next);
     }
-    kv_cnt += n;
     if (!ok) break;
+    if (ahead) umma_commit(&sm.q_empty[qs_nx]);
+    kv_cnt = kv_next;
+    u = nx;
+    s_issued = ahead;
   }
   // every MMA issued so far completes before TMEM is released
   umma_commit(&sm.drain);
@@ -295,16 +436,16 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
   for (;;) {
     const int slot = it_cnt & 1;
     if (!WS_WAIT_WARP(&sm.item_full[slot], (it_cnt >> 1) & 1)) break;
-    const WorkItem it = sm.items[slot];
+    const int valid = sm.items[slot].valid;
+    const WsTile tt = sm.items[slot].t[tile];
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
     ++it_cnt;
-    if (!it.valid) break;
-    const ItemGeom g = item_geom(it, p);
-    const SeqInfo& s = it.seq;
-    const int ni = g.n[tile];
-    const int rows = g.rows[tile];
-    const int qt0 = g.q0 + kTileM * tile;             // first query position of this tile
+    if (!valid) break;
+    const SeqInfo& s = tt.seq;
+    const int ni = tt.n;
+    const int qt0 = tt.q0;                            // first query position of this tile
+    const int rows = s.q_len - qt0;                   // valid rows of the tile (may exceed 128)
     const int qpos = qt0 + row;
 
     float m_run = -INFINITY;
@@ -406,7 +547,7 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
 
     // ---- epilogue ----
     const bool row_ok = row < rows;
-    DT* dst = static_cast<DT*>(p.out) + ((size_t)(s.q_start + (row_ok ? qpos : 0)) * p.Hq + it.h) * (size_t)p.d;
+    DT* dst = static_cast<DT*>(p.out) + ((size_t)(s.q_start + (row_ok ? qpos : 0)) * p.Hq + tt.h) * (size_t)p.d;
     if (ni > 0) {
       if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt - 1) & 1)) break;
       tc_fence_after();
@@ -430,11 +571,11 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
           }
         }
       }
-      if (row_ok && p.lse) p.lse[(size_t)it.h * p.T + s.q_start + qpos] = m_run * p.scale + logf(l_e);
+      if (row_ok && p.lse) p.lse[(size_t)tt.h * p.T + s.q_start + qpos] = m_run * p.scale + logf(l_e);
     } else if (row_ok) {
 #pragma unroll
       for (int col = 0; col < DP; col += 8) *reinterpret_cast<uint4*>(dst + col) = make_uint4(0u, 0u, 0u, 0u);
-      if (p.lse) p.lse[(size_t)it.h * p.T + s.q_start + qpos] = -INFINITY;
+      if (p.lse) p.lse[(size_t)tt.h * p.T + s.q_start + qpos] = -INFINITY;
     }
     tc_fence_before();
   }
