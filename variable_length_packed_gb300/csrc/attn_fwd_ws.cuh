@@ -417,6 +417,128 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   drain_wait(&sm.drain, 0);
 }
 
+// P for 32 keys of one row: exp2(S * scale_log2 - mb), rounded to the input
+// type and packed in pairs, with the rounded and the exact running sums.
+template <typename DT>
+__device__ __forceinline__ void ws_exp_chunk(const uint32_t* sr, uint32_t* pk, float2 scale2, float2 bias2, float2& lr_a,
+                                             float2& lr_b, float2& le_a, float2& le_b) {
+  using Tr = DTypeTraits<DT>;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float2 arg =
+        __ffma2_rn(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2, bias2);
+    const float x0 = ex2_approx(arg.x);
+    const float x1 = ex2_approx(arg.y);
+    pk[e] = Tr::pack2(x0, x1);
+    if (e & 1) {
+      le_b = __fadd2_rn(le_b, make_float2(x0, x1));
+      Tr::acc2(pk[e], lr_b.x, lr_b.y);
+    } else {
+      le_a = __fadd2_rn(le_a, make_float2(x0, x1));
+      Tr::acc2(pk[e], lr_a.x, lr_a.y);
+    }
+  }
+}
+
+// Last visible column of KV tile j (keys from kv0) for query position qpos
+// (negative: none; rows past the sequence see none).
+__device__ __forceinline__ int ws_row_lim(const SeqInfo& s, int qpos, bool row_valid, int kv0) {
+  return row_valid ? (s.causal ? min(s.kv_len - 1, qpos + s.shift) : s.kv_len - 1) - kv0 : -1;
+}
+
+// Softmax of one KV tile for one row (the calling thread's TMEM lane): S from
+// TMEM, online max / sums, P (rounded to the input type) back over S in two
+// halves of 64 keys, lazy O rescale.  `partial` (tile-uniform): some row of
+// the tile may not see all 128 keys; columns past the row's last visible key
+// are masked, and when no row of the warp sees a key in the second half, its
+// exponentials are skipped and zero P is stored there.
+// Returns false when a wait gave up.
+template <typename DT, int DP>
+__device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams& p, volatile uint32_t* abort_flag,
+                                                uint32_t tS, uint32_t tO, int tile, int j, uint32_t o_cnt, bool partial,
+                                                const SeqInfo& s, int qpos, bool row_valid, float sl2, float& m_run,
+                                                float2& lr_a, float2& lr_b, float2& le_a, float2& le_b) {
+  const int lane = threadIdx.x & 31;
+  const int kv0 = j * kBlockN;
+  uint32_t sr[128];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
+  tmem_ld_wait_regs32(sr);
+  tmem_tie_regs32(sr + 32);
+  tmem_tie_regs32(sr + 64);
+  tmem_tie_regs32(sr + 96);
+  if (partial) {
+    const int lim = ws_row_lim(s, qpos, row_valid, kv0);
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+  }
+  // row max: three-input max, four independent chains
+  float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+    mx0 = fmax3f(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+    mx1 = fmax3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+    mx2 = fmax3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+    mx3 = fmax3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+  }
+  const float m_tile = fmax3f(fmaxf(mx0, mx1), mx2, mx3);
+  const float m_new = fmaxf(m_run, m_tile);
+  const bool need = (m_new - m_run) * sl2 > kRescaleThreshold;   // false while both are -inf
+  float alpha = 1.f;
+  if (need) {
+    alpha = ex2_approx((m_run - m_new) * sl2);
+    m_run = m_new;
+    const float2 a2 = make_float2(alpha, alpha);
+    lr_a = __fmul2_rn(lr_a, a2);
+    lr_b = __fmul2_rn(lr_b, a2);
+    le_a = __fmul2_rn(le_a, a2);
+    le_b = __fmul2_rn(le_b, a2);
+  }
+  const float mb = (m_run == -INFINITY ? 0.f : m_run) * sl2;
+  const float2 scale2 = make_float2(sl2, sl2);
+  const float2 bias2 = make_float2(-mb, -mb);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if (partial && half == 1 &&
+        __all_sync(0xffffffffu, ws_row_lim(s, qpos, row_valid, kv0) < 2 * 32)) {
+      // no row of the warp sees keys 64..127: their P is zero
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = 0u;
+      tmem_st16(tS + 32, pk);
+      tmem_st16(tS + 48, pk);
+    } else {
+#pragma unroll
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
+        uint32_t pk[16];
+        ws_exp_chunk<DT>(sr + 32 * c, pk, scale2, bias2, lr_a, lr_b, le_a, le_b);
+        tmem_st16(tS + 16 * c, pk);
+      }
+    }
+    if (half == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
+      // O_t must hold the previous P V product before it is rescaled, and the
+      // rescaled O must be in TMEM before this tile's first P V step
+      if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_ld_wait_regs32(o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(tO + 32 * c, o);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(half == 0 ? &sm.p_lo[tile] : &sm.p_hi[tile]);
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // warps 2-9: softmax + epilogue, tile = (warp - 2) / 4
 // ---------------------------------------------------------------------------
@@ -456,90 +578,12 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
       if (!WS_WAIT_WARP(&sm.s_full[tile], s_cnt & 1)) { ok = false; break; }
       ++s_cnt;
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
-      tmem_ld_wait_regs32(sr);
-      tmem_tie_regs32(sr + 32);
-      tmem_tie_regs32(sr + 64);
-      tmem_tie_regs32(sr + 96);
-
+      // partial tile: the sequence ends inside it, or it crosses the causal diagonal
       const int kv0 = j * kBlockN;
-      if (kv0 + kBlockN > s.kv_len || (s.causal && kv0 + kBlockN - 1 > qt0 + s.shift)) {
-        // last visible column of this tile for this row (negative: none)
-        const int lim = s.causal ? min(s.kv_len - 1, qpos + s.shift) - kv0 : s.kv_len - 1 - kv0;
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-      }
-      // row max: three-input max, four independent chains
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        mx0 = fmax3f(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
-        mx1 = fmax3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-        mx2 = fmax3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-        mx3 = fmax3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-      }
-      const float m_tile = fmax3f(fmaxf(mx0, mx1), mx2, mx3);
-      const float m_new = fmaxf(m_run, m_tile);
-      const bool need = (m_new - m_run) * sl2 > kRescaleThreshold;   // false while both are -inf
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx((m_run - m_new) * sl2);
-        m_run = m_new;
-        const float2 a2 = make_float2(alpha, alpha);
-        lr_a = __fmul2_rn(lr_a, a2);
-        lr_b = __fmul2_rn(lr_b, a2);
-        le_a = __fmul2_rn(le_a, a2);
-        le_b = __fmul2_rn(le_b, a2);
-      }
-      const float mb = (m_run == -INFINITY ? 0.f : m_run) * sl2;
-      const float2 scale2 = make_float2(sl2, sl2);
-      const float2 bias2 = make_float2(-mb, -mb);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 arg = __ffma2_rn(
-                make_float2(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1])), scale2,
-                bias2);
-            const float x0 = ex2_approx(arg.x);
-            const float x1 = ex2_approx(arg.y);
-            pk[e] = Tr::pack2(x0, x1);
-            if (e & 1) {
-              le_b = __fadd2_rn(le_b, make_float2(x0, x1));
-              Tr::acc2(pk[e], lr_b.x, lr_b.y);
-            } else {
-              le_a = __fadd2_rn(le_a, make_float2(x0, x1));
-              Tr::acc2(pk[e], lr_a.x, lr_a.y);
-            }
-          }
-          tmem_st16(tS + 16 * c, pk);
-        }
-        if (half == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
-          // O_t must hold the previous P V product before it is rescaled, and the
-          // rescaled O must be in TMEM before this tile's first P V step
-          if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < DP / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_ld_wait_regs32(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + 32 * c, o);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(half == 0 ? &sm.p_lo[tile] : &sm.p_hi[tile]);
-      }
+      const bool masked = kv0 + kBlockN > s.kv_len || (s.causal && kv0 + kBlockN - 1 > qt0 + s.shift);
+
+      ok = ws_softmax_tile<DT, DP>(sm, p, abort_flag, tS, tO, tile, j, o_cnt, masked, s, qpos, row < rows, sl2, m_run,
+                                   lr_a, lr_b, le_a, le_b);
       if (!ok) break;
     }
     if (!ok) break;
