@@ -377,34 +377,75 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     if (!fetch(nx)) break;
     const bool ahead = nx.valid && nx.paired && nx.n_all > 0;
     const uint32_t kv_next = kv_cnt + u.n_all;
-    int qs_nx = 0;
-    if (ahead) {
-      qs_nx = q_cnt % kQSlots;
-      if (!WS_WAIT(&sm.q_full[qs_nx], (q_cnt / kQSlots) & 1)) break;
-      ++q_cnt;
-    }
+    const int qs_nx = q_cnt % kQSlots;
+    const uint32_t q_par_nx = (q_cnt / kQSlots) & 1;
+    if (ahead) ++q_cnt;
+    bool q_nx_ready = !ahead;   // nx's Q tiles landed
+    // The two tiles move through P V (two halves) and then nx's S MMA in the
+    // order their inputs become ready, so a tile whose softmax finished first
+    // waits neither for the other tile nor for loads queued behind it.
+    int state[2];          // 1: first P V half pending, 2: second half, 3: S of nx, 0: done
+    int st[2], st_nx[2];
+    uint32_t par[2], vpar[2], kpar_nx[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      if (ok && u.t[t].n > 0) {
-        const uint32_t c = kv_cnt + ((t == 1 && u.t[0].n > 0) ? 1u : 0u);
-        const int st = c % kWsStages;
-        const uint32_t vs = v_lo0 + st * kStep;
-        const uint32_t par = p_cnt[t] & 1;
-        ++p_cnt[t];
-        ok = WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1) && WS_WAIT(&sm.p_lo[t], par);
-        if (ok) {
+      const bool s_next = ahead && nx.t[t].n > 0;
+      state[t] = u.t[t].n > 0 ? 1 : (s_next ? 3 : 0);
+      const uint32_t c = kv_cnt + ((t == 1 && u.t[0].n > 0) ? 1u : 0u);
+      st[t] = c % kWsStages;
+      vpar[t] = (c / kWsStages) & 1;
+      par[t] = p_cnt[t] & 1;
+      if (u.t[t].n > 0) ++p_cnt[t];
+      const uint32_t cn = kv_next + ((t == 1 && nx.t[0].n > 0) ? 1u : 0u);
+      st_nx[t] = cn % kWsStages;
+      kpar_nx[t] = (cn / kWsStages) & 1;
+    }
+    uint32_t idle = 0;
+    uint64_t idle_t0 = 0;
+    while (ok && (state[0] | state[1])) {
+      bool progressed = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (state[t] == 1 && mbar_test_wait(&sm.p_lo[t], par[t]) && mbar_test_wait(&sm.v_full[st[t]], vpar[t])) {
           tc_fence_after();
-          issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, false);
-          ok = WS_WAIT(&sm.p_hi[t], par);
+          issue_pv<0, 4>(tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, false);
+          state[t] = 2;
+          progressed = true;
         }
-        if (ok) {
+        if (state[t] == 2 && mbar_test_wait(&sm.p_hi[t], par[t])) {
           tc_fence_after();
-          issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
+          issue_pv<4, 8>(tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, true);
           umma_commit(&sm.o_full[t]);
-          umma_commit(&sm.v_empty[st]);
+          umma_commit(&sm.v_empty[st[t]]);
+          state[t] = (ahead && nx.t[t].n > 0) ? 3 : 0;
+          progressed = true;
+        }
+        if (state[t] == 3) {
+          if (!q_nx_ready) q_nx_ready = mbar_test_wait(&sm.q_full[qs_nx], q_par_nx);
+          if (q_nx_ready && mbar_test_wait(&sm.k_full[st_nx[t]], kpar_nx[t])) {
+            tc_fence_after();
+            issue_qk<DP>(tS[t], q_lo00 + qs_nx * 2 * kStep + t * kStep, k_lo0 + st_nx[t] * kStep, idesc_qk);
+            umma_commit(&sm.s_full[t]);
+            umma_commit(&sm.k_empty[st_nx[t]]);
+            state[t] = 0;
+            progressed = true;
+          }
         }
       }
-      if (ok && ahead && nx.t[t].n > 0) ok = pair_s(nx, t, q_lo00 + qs_nx * 2 * kStep, kv_next);
+      if (progressed) {
+        idle = 0;
+        idle_t0 = 0;
+      } else if ((++idle & 255u) == 0) {   // bounded polling, like the other waits
+        if (*abort_flag) { ok = false; break; }
+        const uint64_t now = globaltimer_ns();
+        if (idle_t0 == 0) {
+          idle_t0 = now;
+        } else if (now - idle_t0 > kWaitLimitNs) {
+          *abort_flag = 1u;
+          atomicOr(p.status, THD_WAIT_TIMEOUT_BIT);
+          ok = false;
+        }
+      }
     }
     if (!ok) break;
     if (ahead) umma_commit(&sm.q_empty[qs_nx]);
