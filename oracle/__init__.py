@@ -26,8 +26,8 @@ Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 case counts).  Nothing is "parity unpinned".
 """
 from .attention import (thd_attention_fwd, thd_attention_rows, sequence_spans, thd_attention_fwd_general,
-                        merge_partials, visible_keys, thd_attention_bwd, MASK_PADDING, MASK_PADDING_CAUSAL,
-                        MASK_PADDING_CAUSAL_BOTTOM_RIGHT)
+                        merge_partials, visible_keys, visible_range, thd_attention_bwd, MASK_PADDING,
+                        MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT)
 from .mask import (padding_mask_loop, padding_mask_formula, padding_mask_cross_loop,
                    padding_mask_cross_formula)
 
@@ -39,6 +39,7 @@ __all__ = [
     "merge_partials",
     "thd_attention_bwd",
     "visible_keys",
+    "visible_range",
     "MASK_PADDING",
     "MASK_PADDING_CAUSAL",
     "MASK_PADDING_CAUSAL_BOTTOM_RIGHT",

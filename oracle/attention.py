@@ -157,15 +157,38 @@ def visible_keys(i, Lq, Lkv, mask_type):
     return int(min(Lkv, max(0, i + shift + 1)))
 
 
+def visible_range(i, Lq, Lkv, mask_type, window=(-1, -1)):
+    """Keys [lo, hi) of a sequence visible to query position i, with a sliding window.
+
+    The pages name sliding windows only as an option the per-sequence policy PR rejects
+    ("Add per-sequence causal policy to packed THD attention", Changes); the window is read
+    here as a band around the diagonal the sequence's mask type uses: with
+    shift = Lkv - Lq for bottom-right alignment and 0 otherwise, key j is visible iff it is
+    visible under the mask type (visible_keys) and
+        i + shift - left <= j <= i + shift + right,
+    a negative ``left`` / ``right`` leaving that side unbounded.  (-1, -1) is no window.
+    Returns (lo, hi) with lo == hi when no key is visible.
+    """
+    left, right = int(window[0]), int(window[1])
+    hi = visible_keys(i, Lq, Lkv, mask_type)
+    shift = (Lkv - Lq) if mask_type == MASK_PADDING_CAUSAL_BOTTOM_RIGHT else 0
+    if right >= 0:
+        hi = min(hi, max(0, i + shift + right + 1))
+    lo = max(0, i + shift - left) if left >= 0 else 0
+    return lo, max(lo, hi)
+
+
 def thd_attention_fwd_general(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
-                              cu_seqlens_kv_padded, mask_type, batch_size, softmax_scale):
+                              cu_seqlens_kv_padded, mask_type, batch_size, softmax_scale,
+                              window=(-1, -1)):
     """Packed attention with separate query and key/value sequences.
 
     Query sequence b is rows [sq_b, sq_b + Lq_b) of q, its key/value sequence rows
     [sk_b, sk_b + Lkv_b) of k and v (same packing rules as thd_attention_fwd).  Query i
-    sees the first visible_keys(i, ...) keys of its sequence.  Rows that see no key, and
-    rows of no sequence, get out = 0 and lse = -inf.  mask_type: per-sequence codes
-    (None = all MASK_PADDING).  Returns (out [Tq, Hq, d], lse [Hq, Tq]) in fp64.
+    sees the keys visible_range(i, ...) of its sequence (a prefix, visible_keys, without
+    a window).  Rows that see no key, and rows of no sequence, get out = 0 and lse = -inf.
+    mask_type: per-sequence codes (None = all MASK_PADDING).  window: (left, right), see
+    visible_range.  Returns (out [Tq, Hq, d], lse [Hq, Tq]) in fp64.
     """
     q, k, v = _as64(q), _as64(k), _as64(v)
     Tq, Hq, d = q.shape
@@ -180,21 +203,21 @@ def thd_attention_fwd_general(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q
         Lq, Lkv = int(ql[b]), int(kl[b])
         if Lq <= 0:
             continue
-        nvis = np.array([visible_keys(i, Lq, max(Lkv, 0), int(codes[b])) for i in range(Lq)])
+        ranges = [visible_range(i, Lq, max(Lkv, 0), int(codes[b]), window) for i in range(Lq)]
         for h in range(Hq):
             g = h // group
             qq = q[qs[b]:qs[b] + Lq, h, :]
             kk = k[ks[b]:ks[b] + max(Lkv, 0), g, :]
             vv = v[ks[b]:ks[b] + max(Lkv, 0), g, :]
             for i in range(Lq):
-                n = nvis[i]
-                if n == 0:
+                lo, hi = ranges[i]
+                if hi == lo:
                     continue
-                z = softmax_scale * (kk[:n] @ qq[i])
+                z = softmax_scale * (kk[lo:hi] @ qq[i])
                 zmax = z.max()
                 e = np.exp(z - zmax)
                 s = e.sum()
-                out[qs[b] + i, h, :] = (e / s) @ vv[:n]
+                out[qs[b] + i, h, :] = (e / s) @ vv[lo:hi]
                 lse[h, qs[b] + i] = zmax + np.log(s)
     return out, lse
 
@@ -225,7 +248,7 @@ def merge_partials(out_a, lse_a, out_b, lse_b):
 # ---------------------------------------------------------------------------------------------
 
 def thd_attention_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
-                      cu_seqlens_kv_padded, mask_type, batch_size, softmax_scale):
+                      cu_seqlens_kv_padded, mask_type, batch_size, softmax_scale, window=(-1, -1)):
     """dQ, dK, dV of out = softmax(scale q k^T [masked]) v for every sequence and head.
 
     "Add per-sequence causal policy to packed THD attention" (Changes, Validation) checks
@@ -238,7 +261,8 @@ def thd_attention_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_p
 
     Grouped-query heads: dK / dV of a key/value head sum the contributions of every query
     head that reads it.  Rows of no sequence, rows that see no key and keys no query sees
-    get zero gradient.  Returns (dq [Tq,Hq,d], dk [Tkv,Hkv,d], dv [Tkv,Hkv,d]) in fp64.
+    get zero gradient.  window: (left, right) as in visible_range.  Returns
+    (dq [Tq,Hq,d], dk [Tkv,Hkv,d], dv [Tkv,Hkv,d]) in fp64.
     """
     q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
     Tq, Hq, d = q.shape
@@ -255,9 +279,10 @@ def thd_attention_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_p
         Lq, Lkv = int(ql[b]), int(kl[b])
         if Lq <= 0 or Lkv <= 0:
             continue
-        nvis = np.array([visible_keys(i, Lq, Lkv, int(codes[b])) for i in range(Lq)])
-        visible = np.arange(Lkv)[None, :] < nvis[:, None]
-        rows = nvis > 0
+        ranges = np.array([visible_range(i, Lq, Lkv, int(codes[b]), window) for i in range(Lq)])
+        keys = np.arange(Lkv)[None, :]
+        visible = (keys >= ranges[:, :1]) & (keys < ranges[:, 1:])
+        rows = ranges[:, 1] > ranges[:, 0]
         sq, sk = slice(qs[b], qs[b] + Lq), slice(ks[b], ks[b] + Lkv)
         for h in range(Hq):
             g = h // group

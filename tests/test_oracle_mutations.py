@@ -138,3 +138,56 @@ def test_general_pins_catch_mutant(monkeypatch, target, mutant):
         except (AssertionError, ValueError, IndexError):
             failed += 1
     assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
+
+
+import test_oracle_window as win
+
+WINDOW_PINS = [
+    lambda: [win.test_band_against_torch_tril_triu(lq, lkv, code, w) for lq, lkv in ((11, 11), (6, 13))
+             for code in (0, 1, 2) for w in ((3, -1), (-1, 2), (2, 4))],
+    lambda: [win.test_zero_width_window_copies_one_value_row(*c) for c in ((9, 9, 0), (5, 12, 2))],
+    lambda: win.test_causal_window_is_full_attention_over_the_last_keys(4),
+]
+
+
+def window_lower_off_by_one(i, Lq, Lkv, mask_type, window=(-1, -1)):
+    left, right = window
+    hi = oa.visible_keys(i, Lq, Lkv, mask_type)
+    shift = (Lkv - Lq) if mask_type == 2 else 0
+    if right >= 0:
+        hi = min(hi, max(0, i + shift + right + 1))
+    lo = max(0, i + shift - left + 1) if left >= 0 else 0   # mistake: one key too few on the left
+    return lo, max(lo, hi)
+
+
+def window_upper_exclusive(i, Lq, Lkv, mask_type, window=(-1, -1)):
+    left, right = window
+    hi = oa.visible_keys(i, Lq, Lkv, mask_type)
+    shift = (Lkv - Lq) if mask_type == 2 else 0
+    if right >= 0:
+        hi = min(hi, max(0, i + shift + right))             # mistake: right edge excluded
+    lo = max(0, i + shift - left) if left >= 0 else 0
+    return lo, max(lo, hi)
+
+
+def window_ignores_alignment(i, Lq, Lkv, mask_type, window=(-1, -1)):
+    left, right = window
+    hi = oa.visible_keys(i, Lq, Lkv, mask_type)
+    if right >= 0:
+        hi = min(hi, max(0, i + right + 1))                 # mistake: band not moved to the
+    lo = max(0, i - left) if left >= 0 else 0               # bottom-right diagonal
+    return lo, max(lo, hi)
+
+
+@pytest.mark.parametrize("mutant", [window_lower_off_by_one, window_upper_exclusive, window_ignores_alignment])
+def test_window_pins_catch_mutant(monkeypatch, mutant):
+    import oracle as pkg
+    monkeypatch.setattr(oa, "visible_range", mutant)
+    monkeypatch.setattr(pkg, "visible_range", mutant)
+    failed = 0
+    for pin in WINDOW_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
