@@ -112,6 +112,34 @@ int thd_attn_fwd(const void* q, const void* k, const void* v,
                  int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * thd_attn_fwd_window — thd_attn_fwd with a sliding window (local attention).
+ *
+ * Source: the window is named only as an option the per-sequence policy PR
+ * rejects ("Add per-sequence causal policy to packed THD attention", Changes);
+ * it is taken as a band around the diagonal of each sequence's mask type.
+ * With shift = Lkv - Lq for bottom-right sequences (mask type 2) and 0
+ * otherwise, key j of a sequence is visible to its query i iff it is visible
+ * under the sequence's mask type and
+ *     i + shift - window_left <= j <= i + shift + window_right.
+ * window_left, window_right  >= -1; -1 leaves that side unbounded, so
+ *              (-1, -1) is exactly thd_attn_fwd.  A causal mask type already
+ *              bounds the right side at the diagonal.
+ * Every other argument, the results on pad rows and rows that see no key, and
+ * the errors are those of thd_attn_fwd (THD_ERR_ARG also for an extent < -1).
+ * Work scales with the window: KV tiles outside every row's band of a query
+ * tile are not visited.
+ */
+int thd_attn_fwd_window(const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                        const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                        const uint8_t* seq_is_causal,
+                        int batch_size, int max_seqlen, float softmax_scale,
+                        void* out, float* lse,
+                        int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                        int dtype, int window_left, int window_right,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * thd_attn_bwd_workspace_size — bytes of device workspace thd_attn_bwd needs for
  * T = total_tokens rows, Hq query heads and head_dim d:
  * 256 + (Hq*T*4 rounded up to 256) + (T*Hq*d*4 rounded up to 256); 0 for invalid sizes.
@@ -153,6 +181,23 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
                  void* dq, void* dk, void* dv,
                  int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
                  int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * thd_attn_bwd_window — thd_attn_bwd for a forward computed with
+ * thd_attn_fwd_window: the same window_left / window_right (>= -1, -1 =
+ * unbounded; (-1, -1) is exactly thd_attn_bwd).  Keys outside every query's
+ * band get exact zero dK / dV.  Other arguments and errors as thd_attn_bwd.
+ */
+int thd_attn_bwd_window(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                        const void* dout,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                        const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                        const uint8_t* seq_is_causal,
+                        int batch_size, int max_seqlen, float softmax_scale,
+                        void* dq, void* dk, void* dv,
+                        int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                        int dtype, int window_left, int window_right,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * thd_attn_fwd_noalloc — thd_attn_fwd for callers that cannot allocate device

@@ -122,3 +122,24 @@ def test_bwd_and_merge_arguments_rejected_before_launch(lib):
     assert lib.thd_padding_mask_cross(P(16), P(16), -1, 4, 4, P(16), P(16), P(None)) == -1
     assert lib.thd_padding_mask_cross(P(16), P(16), 0, 4, 4, P(None), P(None), P(None)) == 0
     assert lib.thd_padding_mask_cross(P(None), P(16), 2, 4, 4, P(16), P(16), P(None)) == -1
+
+
+def test_window_arguments_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    F = ctypes.c_float
+
+    def fwd(left, right, T=8):
+        return lib.thd_attn_fwd_window(P(16), P(16), P(16), P(16), P(16), P(None), P(None), P(None), 1, 8, F(0.125),
+                                       P(16), P(None), T, 2, 2, 64, 0, left, right, P(16), ctypes.c_size_t(256),
+                                       P(None))
+    assert fwd(-2, -1) == -1 and fwd(0, -5) == -1
+    assert fwd(-1, -1, T=0) == 0 and fwd(3, 0, T=0) == 0      # valid windows, nothing to do
+
+    def bwd(left, right):
+        ws = lib.thd_attn_bwd_workspace_size(100, 4, 128)
+        return lib.thd_attn_bwd_window(P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(None), P(None),
+                                       P(None), 1, 8, F(0.1), P(16), P(16), P(16), 100, 4, 2, 128, 0, left, right,
+                                       P(256), ctypes.c_size_t(ws), P(None))
+    assert bwd(-3, 0) == -1 and bwd(2, -2) == -1
+    with pytest.raises(ValueError):
+        vlp._window_args((-2, 0))

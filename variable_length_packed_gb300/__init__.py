@@ -50,10 +50,15 @@ def load_library():
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.thd_attn_fwd.restype = I
     lib.thd_attn_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P, SZ, P]
+    lib.thd_attn_fwd_window.restype = I
+    lib.thd_attn_fwd_window.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, I, I, P, SZ, P]
     lib.thd_attn_fwd_noalloc.restype = I
     lib.thd_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P]
     lib.thd_attn_bwd.restype = I
     lib.thd_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, F, P, P, P, I, I, I, I, I, P, SZ, P]
+    lib.thd_attn_bwd_window.restype = I
+    lib.thd_attn_bwd_window.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, F, P, P, P, I, I, I, I, I, I, I, P, SZ,
+                                        P]
     lib.thd_attn_bwd_workspace_size.restype = SZ
     lib.thd_attn_bwd_workspace_size.argtypes = [I, I, I]
     lib.thd_attn_merge.restype = I
@@ -98,9 +103,16 @@ def _stream_handle(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _window_args(window):
+    left, right = (int(window[0]), int(window[1]))
+    if left < -1 or right < -1:
+        raise ValueError("window extents must be >= -1 (-1: unbounded)")
+    return left, right
+
+
 def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
                  cu_seqlens_kv_padded=None, seq_is_causal=None, batch_size=None, max_seqlen=0,
-                 softmax_scale=None, out=None, lse=None, return_lse=True, workspace=None):
+                 softmax_scale=None, out=None, lse=None, return_lse=True, workspace=None, window=(-1, -1)):
     """Packed THD self-attention forward on the current CUDA stream.
 
     q: [T, Hq, d], k/v: [T, Hkv, d] (bf16 or fp16, CUDA, contiguous).  cu_seqlens_*:
@@ -108,6 +120,7 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     seq_is_causal: bool/uint8 CUDA tensor [>= batch_size] or None (all full-context), the
     per-sequence mask type: MASK_PADDING (0), MASK_PADDING_CAUSAL (1, top-left) or
     MASK_PADDING_CAUSAL_BOTTOM_RIGHT (2).  q and k/v sequences may differ in length.
+    window: (left, right) sliding window around the mask type's diagonal, -1 = unbounded.
     Returns (out [T, Hq, d], lse [Hq, T] float32 or None).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
@@ -140,13 +153,14 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = torch.empty(thd_attn_workspace_size(), dtype=torch.uint8, device=q.device)
+    left, right = _window_args(window)
     with torch.cuda.device(q.device):
-        st = _lib().thd_attn_fwd(
+        st = _lib().thd_attn_fwd_window(
             _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
             _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), _ptr(seq_is_causal),
             int(batch_size), int(max_seqlen), float(softmax_scale), _ptr(out), _ptr(lse),
             int(T), int(Hq), int(Hkv), int(d), THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16,
-            _ptr(workspace), workspace.numel(), _stream_handle(q.device))
+            left, right, _ptr(workspace), workspace.numel(), _stream_handle(q.device))
     if st != THD_OK:
         raise ThdError(st, "thd_attn_fwd")
     return out, lse
@@ -247,9 +261,9 @@ def thd_padding_mask_cross(cu_seqlens_q, cu_seqlens_kv, batch_size, max_seqlen_q
 
 def thd_attn_bwd(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
                  cu_seqlens_kv_padded=None, seq_is_causal=None, batch_size=None, max_seqlen=0,
-                 softmax_scale=None, dq=None, dk=None, dv=None, workspace=None):
-    """Gradients (dq, dk, dv) of thd_attn_fwd for the same batch; out / lse are the forward's
-    outputs.  head_dim 64 or 128."""
+                 softmax_scale=None, dq=None, dk=None, dv=None, workspace=None, window=(-1, -1)):
+    """Gradients (dq, dk, dv) of thd_attn_fwd for the same batch and window; out / lse are
+    the forward's outputs.  head_dim 64 or 128."""
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout),
                     ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv),
                     ("cu_seqlens_q_padded", cu_seqlens_q_padded),
@@ -270,12 +284,13 @@ def thd_attn_bwd(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlen
     need = int(_lib().thd_attn_bwd_workspace_size(int(T), int(Hq), int(d)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    left, right = _window_args(window)
     with torch.cuda.device(q.device):
-        st = _lib().thd_attn_bwd(
+        st = _lib().thd_attn_bwd_window(
             _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
             _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), _ptr(seq_is_causal), int(batch_size),
             int(max_seqlen), float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), int(T), int(Hq), int(Hkv), int(d),
-            THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16, _ptr(workspace), workspace.numel(),
+            THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16, left, right, _ptr(workspace), workspace.numel(),
             _stream_handle(q.device))
     if st != THD_OK:
         raise ThdError(st, "thd_attn_bwd")

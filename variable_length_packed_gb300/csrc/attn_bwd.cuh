@@ -206,12 +206,13 @@ __global__ void __launch_bounds__(128, 1)
     const int g = it.h, kv0 = it.qblock * kTileM;
     const int keys_valid = min(kTileM, s.kv_len - kv0);
     const int key = kv0 + tid;                       // this thread's key position (TMEM lane)
-    int qt_first = 0;
-    if (s.causal) {
-      const long long first_q = (long long)kv0 - s.shift;   // first query that sees key kv0
-      qt_first = first_q <= 0 ? 0 : (int)(first_q / kTileM);
-    }
-    const int nqt = (s.q_len + kTileM - 1) / kTileM;
+    // query tiles holding a query that sees a key of [kv0, kv0 + 128): query i sees key j
+    // only if i + shift - lo_off <= j <= i + shift + hi_off
+    const long long first_q = (long long)kv0 - s.shift - s.hi_off;
+    const long long last_q = (long long)kv0 + kTileM - 1 - s.shift + s.lo_off;
+    const int qt_first = first_q <= 0 ? 0 : (int)min(first_q / kTileM, (long long)INT32_MAX);
+    const int nqt_all = (s.q_len + kTileM - 1) / kTileM;
+    const int nqt = last_q < 0 ? 0 : (int)min((long long)nqt_all, last_q / kTileM + 1);
     const bool any = s.q_len > 0 && qt_first < nqt;
     if (any && tid == 0) {
       mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
@@ -269,7 +270,12 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after();
 
         // ---- P^T and dS^T for this thread's key row, 32 queries at a time ----
+        // query column c of the tile sees this key iff c_lo <= c <= c_hi (query
+        // q0 + c sees key j iff j - shift - hi_off <= q0 + c <= j - shift + lo_off)
         const bool kvalid = key < s.kv_len;
+        const long long kd = (long long)key - s.shift - q0;
+        const int c_lo = (int)min(max(kd - s.hi_off, -1ll), (long long)kTileM);
+        const int c_hi = (int)max(min(kd + s.lo_off, (long long)rows_q - 1), -1ll);
 #pragma unroll
         for (int c0 = 0; c0 < 4; ++c0) {
           uint32_t sr[32], dr[32];
@@ -284,8 +290,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int c = 32 * c0 + 2 * e + u;
-              const int qpos = q0 + c;
-              const bool vis = kvalid && c < rows_q && (!s.causal || key <= qpos + s.shift);
+              const bool vis = kvalid && c >= c_lo && c <= c_hi;
               const float x = ex2_approx(fmaf(__uint_as_float(sr[2 * e + u]), sl2, -sm.lse2[c]));
               pv[u] = vis ? x : 0.f;
               dsv[u] = pv[u] * (__uint_as_float(dr[2 * e + u]) - sm.dd[c]);

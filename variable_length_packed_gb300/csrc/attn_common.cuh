@@ -41,6 +41,7 @@ struct AttnParams {
   unsigned long long* work_counter;
   uint32_t* status;
   int claim;               // work items taken per atomic on the counter (>= 1)
+  int win_left, win_right; // sliding window (keys before / after the diagonal), -1 = unbounded
   int B, T, Hq, Hkv, d, group;
   float scale;             // softmax scale
   float scale_log2;        // softmax scale * log2(e)
@@ -54,10 +55,40 @@ struct AttnParams {
 constexpr int kMaskPadding = 0;
 constexpr int kMaskCausalBottomRight = 2;
 
+// No bound on that side of the sliding window.
+constexpr int kNoBound = 1 << 30;
+
+// Key j of a sequence is visible to its query i iff 0 <= j < kv_len and
+//   i + shift - lo_off <= j <= i + shift + hi_off,
+// shift being the diagonal of the mask type (kv_len - q_len bottom-right, else 0),
+// hi_off = 0 for the causal types (else the window's right extent), lo_off the window's
+// left extent; kNoBound where unbounded.  Without a window this is the prefix the mask
+// type allows.
 struct SeqInfo {
   int q_start, kv_start, q_len, kv_len, causal;
-  int shift;   // causal visibility offset: key j visible to query i iff j <= i + shift
+  int shift;
+  int lo_off, hi_off;
 };
+
+__device__ __forceinline__ void set_visibility(SeqInfo& s, int code, const AttnParams& p) {
+  s.causal = code != kMaskPadding;
+  s.shift = code == kMaskCausalBottomRight ? s.kv_len - s.q_len : 0;
+  const int wr = p.win_right >= 0 ? p.win_right : kNoBound;
+  s.hi_off = s.causal ? 0 : wr;   // min(0, wr): a causal type never looks past the diagonal
+  s.lo_off = p.win_left >= 0 ? p.win_left : kNoBound;
+}
+
+// First / last key of the sequence visible to query position qpos (the first is past the
+// last when none is).  Both grow with qpos, so a block of rows sees keys between the first
+// row's first key and the last row's last key.
+__device__ __forceinline__ int seq_first_key(const SeqInfo& s, int qpos) {
+  const long long f = (long long)qpos + s.shift - s.lo_off;
+  return f < 0 ? 0 : (f > s.kv_len ? s.kv_len : (int)f);
+}
+__device__ __forceinline__ int seq_last_key(const SeqInfo& s, int qpos) {
+  const long long l = (long long)qpos + s.shift + s.hi_off;
+  return l > s.kv_len - 1 ? s.kv_len - 1 : (l < -1 ? -1 : (int)l);
+}
 
 // Sequence b's rows, clamped to the packed buffer [0, T): garbage metadata
 // gives garbage output but never an out-of-range address.
@@ -77,24 +108,20 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
   s.q_len = (int)ql;
   s.kv_len = (int)kl;
   const int code = p.causal ? (int)p.causal[b] : kMaskPadding;
-  s.causal = code != kMaskPadding;
-  s.shift = code == kMaskCausalBottomRight ? s.kv_len - s.q_len : 0;
+  set_visibility(s, code, p);
   return s;
 }
 
-// Number of KV tiles a Q tile whose first row is sequence position q0 must
-// visit: all keys for a full-context sequence, keys up to the last key visible
-// to the tile's last valid row for a causal one.  0 when no row sees a key.
+// KV tiles a Q tile whose first row is sequence position q0 must visit: tiles
+// [kv_first_tile, kv_tiles_for), up to the last key visible to the tile's last valid row
+// and from the first key visible to its first row.  kv_tiles_for is 0 when no row sees a
+// key; the range is empty when kv_first_tile >= kv_tiles_for.
 __device__ __forceinline__ int kv_tiles_for(const SeqInfo& s, int q0, int rows) {
   if (s.kv_len <= 0) return 0;
-  int last = s.kv_len - 1;
-  if (s.causal) {
-    const long long qlast = (long long)min(q0 + rows, s.q_len) - 1 + s.shift;
-    last = (int)(qlast < last ? qlast : last);
-    if (last < 0) return 0;
-  }
-  return last / kBlockN + 1;
+  const int last = seq_last_key(s, min(q0 + rows, s.q_len) - 1);
+  return last < 0 ? 0 : last / kBlockN + 1;
 }
+__device__ __forceinline__ int kv_first_tile(const SeqInfo& s, int q0) { return seq_first_key(s, q0) / kBlockN; }
 
 // ----------------------------------------------------------------------------
 // Tile scheduler.  Work item = (sequence, query head, block of BLOCK_M query
@@ -141,6 +168,7 @@ __device__ __forceinline__ bool seq_is_short(const SeqInfo& s) {
 template <bool kPairs = false>
 __device__ __forceinline__ uint32_t seq_sort_key(const SeqInfo& s) {
   int nkv = (s.kv_len + kBlockN - 1) / kBlockN;
+  if (s.lo_off < kNoBound) nkv = min(nkv, s.lo_off / kBlockN + 2);   // a window bounds the tiles per row block
   if (!kPairs) {
     nkv = nkv > 511 ? 511 : nkv;
     return (uint32_t)(nkv * 2 + (s.causal ? 0 : 1));
@@ -172,15 +200,14 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
 }
 
 // Sequence info of chunk-local sequence i, from the chunk's cache (no global loads).
-__device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i) {
+__device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i, const AttnParams& p) {
   const int4 sp = s.span[i];
   SeqInfo si;
   si.q_start = sp.x;
   si.q_len = sp.y;
   si.kv_start = sp.z;
   si.kv_len = sp.w;
-  si.causal = s.code[i] != kMaskPadding;
-  si.shift = s.code[i] == kMaskCausalBottomRight ? sp.w - sp.y : 0;
+  set_visibility(si, s.code[i], p);
   return si;
 }
 
@@ -236,7 +263,7 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
     const int j = j0 + lane;
     uint32_t it = 0u;
     if (j < n) {
-      const SeqInfo sj = cached_seq(s, s.order[j]);
+      const SeqInfo sj = cached_seq(s, s.order[j], p);
       it = (kPairs && seq_is_short(sj)) ? 0u : seq_items<BLOCK_M, kKvSide>(sj, p);
     }
     const uint32_t incl = warp_incl_scan(it);
@@ -309,7 +336,7 @@ __device__ WorkItem sched_decode(SchedSmem& s, const AttnParams& p, unsigned lon
   const uint32_t local = (uint32_t)(w - s.item_base);
   const int lo = sched_find(s, local);
   it.b = s.chunk_base + s.order[lo];
-  it.seq = cached_seq(s, s.order[lo]);
+  it.seq = cached_seq(s, s.order[lo], p);
   const uint32_t r = local - s.cum[lo];
   const int len = kKvSide ? it.seq.kv_len : it.seq.q_len;
   const uint32_t nblk = (uint32_t)((len + BLOCK_M - 1) / BLOCK_M);

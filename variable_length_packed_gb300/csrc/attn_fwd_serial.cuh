@@ -105,7 +105,10 @@ __global__ void __launch_bounds__(128, 1)
     const int q0 = it.qblock * kTileM;                  // first query position of the tile
     const int rows_valid = min(kTileM, s.q_len - q0);
     const int kvh = it.h / p.group;
-    const int nkv = kv_tiles_for(s, q0, kTileM);
+    // KV tiles [j0, nkv) hold the keys the tile's rows see
+    int nkv = kv_tiles_for(s, q0, kTileM);
+    int j0 = kv_first_tile(s, q0);
+    if (nkv <= j0) nkv = j0 = 0;
     const int qpos = q0 + tid;                          // this thread's query position
 
     // l_run: sum of the P values as rounded for the P V product (normalises O, so each
@@ -121,19 +124,20 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
           for (int pn = 0; pn < kPanels; ++pn) {
             tma_load_2d(sm.q + pn * 16384, &tm_q, &sm.bar_load, it.h * p.d + pn * 64, s.q_start + q0);
-            tma_load_2d(sm.k + pn * 16384, &tm_k, &sm.bar_load, kvh * p.d + pn * 64, s.kv_start);
-            tma_load_2d(sm.v + pn * 16384, &tm_v, &sm.bar_load, kvh * p.d + pn * 64, s.kv_start);
+            tma_load_2d(sm.k + pn * 16384, &tm_k, &sm.bar_load, kvh * p.d + pn * 64, s.kv_start + j0 * kBlockN);
+            tma_load_2d(sm.v + pn * 16384, &tm_v, &sm.bar_load, kvh * p.d + pn * 64, s.kv_start + j0 * kBlockN);
           }
         }
       } else {
+        const int kvr = j0 * kBlockN;
         load_tile_manual<DP>(sm.q, p.q, s.q_start + q0, rows_valid, p.Hq, it.h, p.d, p.T);
-        load_tile_manual<DP>(sm.k, p.k, s.kv_start, min(kBlockN, s.kv_len), p.Hkv, kvh, p.d, p.T);
-        load_tile_manual<DP>(sm.v, p.v, s.kv_start, min(kBlockN, s.kv_len), p.Hkv, kvh, p.d, p.T);
+        load_tile_manual<DP>(sm.k, p.k, s.kv_start + kvr, min(kBlockN, s.kv_len - kvr), p.Hkv, kvh, p.d, p.T);
+        load_tile_manual<DP>(sm.v, p.v, s.kv_start + kvr, min(kBlockN, s.kv_len - kvr), p.Hkv, kvh, p.d, p.T);
         fence_proxy_async_smem();
         __syncthreads();
       }
 
-      for (int j = 0; j < nkv; ++j) {
+      for (int j = j0; j < nkv; ++j) {
         const int kv0 = j * kBlockN;
         // ---- S = Q K^T ----
         if (tid == 0) {
@@ -163,15 +167,17 @@ __global__ void __launch_bounds__(128, 1)
         tmem_tie_regs32(sr + 64);
         tmem_tie_regs32(sr + 96);
 
-        const bool need_mask = (kv0 + kBlockN > s.kv_len) || (s.causal && kv0 + kBlockN - 1 > q0 + s.shift);
+        const long long d0 = (long long)q0 + s.shift;
+        const bool need_mask = (kv0 + kBlockN > s.kv_len) || (kv0 + kBlockN - 1 > d0 + s.hi_off) ||
+                               (kv0 < d0 + (kTileM - 1) - s.lo_off);
+        const int key_lo = seq_first_key(s, qpos), key_hi = seq_last_key(s, qpos);
         float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           float x = __uint_as_float(sr[c]);
           if (need_mask) {
             const int kp = kv0 + c;
-            const bool ok = kp < s.kv_len && (!s.causal || kp <= qpos + s.shift);
-            x = ok ? x : -INFINITY;
+            x = (kp >= key_lo && kp <= key_hi) ? x : -INFINITY;
             sr[c] = __float_as_uint(x);
           }
           mx = fmaxf(mx, x);
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(128, 1)
         m_run = m_new;
 
         // ---- rescale O (after the previous P V has completed) ----
-        if (j > 0) {
+        if (j > j0) {
 #pragma unroll
           for (int c = 0; c < DP / 32; ++c) {
             uint32_t o[32];
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(128, 1)
             const uint32_t voff = kk * 16 * 128;   // 16 key rows of 128 bytes
             umma_ss(tO, smem_desc_sw128(smem_u32(sm.p) + poff, 16, 1024),
                     smem_desc_sw128(smem_u32(sm.v) + voff, 16384, 1024), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+                    (j > j0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&sm.bar_mma);
         }

@@ -52,7 +52,7 @@ struct WsTile {
   SeqInfo seq;   // the tile's sequence
   int h;         // query head
   int q0;        // sequence position of the tile's first query row
-  int n;         // KV tiles the tile visits (0: no row sees a key)
+  int j0, n;     // KV tiles the tile visits: [j0, n); n = 0 when no row sees a key
 };
 
 // Work unit: one block of 256 query rows of a long sequence (two tiles sharing
@@ -61,9 +61,27 @@ struct WsTile {
 struct WsUnit {
   int valid;
   int paired;
-  int n_all;     // K/V tiles loaded for the unit: max(n) shared, n0 + n1 paired
+  int jb;        // first KV tile loaded (shared: the smallest j0 of the tiles with work)
+  int n_all;     // K/V tiles loaded for the unit: max(n) - jb shared, n0 + n1 paired
   WsTile t[2];
 };
+
+// What the MMA warp needs of a unit (the sequences' positions stay with the
+// producer and the softmax warps).
+struct MmaUnit {
+  int valid, paired, jb, n_all;
+  int j0[2], n[2];
+};
+
+// KV tile range of a Q tile, [j0, n), normalised to (0, 0) when empty.  kWin:
+// the call has a sliding window (without one every visited range starts at 0).
+template <bool kWin>
+__device__ __forceinline__ void ws_tile_range(WsTile& tt) {
+  const SeqInfo& s = tt.seq;
+  tt.n = s.q_len > tt.q0 ? kv_tiles_for(s, tt.q0, kTileM) : 0;
+  tt.j0 = kWin ? kv_first_tile(s, tt.q0) : 0;
+  if (tt.n <= tt.j0) tt.n = tt.j0 = 0;
+}
 
 template <int DP>
 struct WsSmem {
@@ -87,10 +105,12 @@ struct WsSmem {
 // within a CTA).  Units of a chunk: the long sequences' 256-row blocks in the
 // scheduler's order, then the short sequences' (sequence, head) tiles, heads
 // innermost, two per unit.
+template <bool kWin>
 __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
   WsUnit u;
   u.valid = 0;
   u.paired = 0;
+  u.jb = 0;
   u.n_all = 0;
   if (!sched_seek<kWsBlockM, false, true>(s, p, w)) return u;
   u.valid = 1;
@@ -98,7 +118,7 @@ __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, u
   const uint32_t n_long_items = s.cum[s.chunk_n];
   if (local < n_long_items) {
     const int pos = sched_find(s, local);
-    const SeqInfo seq = cached_seq(s, s.order[pos]);
+    const SeqInfo seq = cached_seq(s, s.order[pos], p);
     const uint32_t r = local - s.cum[pos];
     const uint32_t nblk = (uint32_t)((seq.q_len + kWsBlockM - 1) / kWsBlockM);
     const int h = (int)(r / nblk);
@@ -108,9 +128,12 @@ __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, u
       u.t[t].seq = seq;
       u.t[t].h = h;
       u.t[t].q0 = qb * kWsBlockM + t * kTileM;
-      u.t[t].n = seq.q_len > u.t[t].q0 ? kv_tiles_for(seq, u.t[t].q0, kTileM) : 0;
+      ws_tile_range<kWin>(u.t[t]);
     }
-    u.n_all = max(u.t[0].n, u.t[1].n);
+    // tile 0's rows come first, so its window starts no later than tile 1's
+    u.jb = !kWin ? 0 : (u.t[0].n > 0 ? u.t[0].j0 : u.t[1].j0);
+    const int jend = max(u.t[0].n, u.t[1].n);
+    u.n_all = jend > u.jb ? jend - u.jb : 0;
   } else {
     u.paired = 1;
     const uint32_t total = (uint32_t)s.n_short * (uint32_t)p.Hq;
@@ -120,15 +143,15 @@ __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, u
       const uint32_t idx = i0 + t;
       WsTile& tt = u.t[t];
       if (idx < total) {
-        tt.seq = cached_seq(s, s.order[s.n_long + (int)(idx / (uint32_t)p.Hq)]);
+        tt.seq = cached_seq(s, s.order[s.n_long + (int)(idx / (uint32_t)p.Hq)], p);
         tt.h = (int)(idx % (uint32_t)p.Hq);
         tt.q0 = 0;
-        tt.n = kv_tiles_for(tt.seq, 0, kTileM);
+        ws_tile_range<kWin>(tt);   // at most KV tile 0
       } else {   // odd count: no second tile
-        tt.seq = SeqInfo{0, 0, 0, 0, 0, 0};
+        tt.seq = SeqInfo{0, 0, 0, 0, 0, 0, kNoBound, kNoBound};
         tt.h = 0;
         tt.q0 = 0;
-        tt.n = 0;
+        tt.j0 = tt.n = 0;
       }
     }
     u.n_all = u.t[0].n + u.t[1].n;
@@ -179,7 +202,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 // warp 0: scheduler + TMA producer
 // ---------------------------------------------------------------------------
-template <int DP>
+template <int DP, bool kWin>
 __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                             const CUtensorMap* tm_v, volatile uint32_t* abort_flag) {
   constexpr uint32_t kTileBytes = WsSmem<DP>::kTileBytes;
@@ -191,7 +214,7 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   Claimer claimer{0ull, 0};
   for (;;) {
     const unsigned long long w = claim_item(claimer, p);
-    WsUnit u = ws_decode(sm.sched, p, w);
+    WsUnit u = ws_decode<kWin>(sm.sched, p, w);
     const int slot = it_cnt & 1;
     if (lane == 0) {
       if (it_cnt >= 2) ok = WS_WAIT(&sm.item_empty[slot], ((it_cnt >> 1) - 1) & 1);
@@ -221,7 +244,7 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
       // sequence (shared), or tile 0's then tile 1's own tile (paired)
       for (int li = 0; ok && li < u.n_all; ++li) {
         const int tsel = (u.paired && !(li == 0 && u.t[0].n > 0)) ? 1 : 0;
-        const int row = u.t[tsel].seq.kv_start + (u.paired ? 0 : li * kBlockN);
+        const int row = u.t[tsel].seq.kv_start + (u.paired ? 0 : (u.jb + li) * kBlockN);
         const int kvh = u.t[tsel].h / p.group;
         const int st = kv_cnt % kWsStages;
         const uint32_t reuse = ((kv_cnt / kWsStages) - 1) & 1;
@@ -258,7 +281,7 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
 // ---------------------------------------------------------------------------
 // warp 1 (one thread): MMA issuer
 // ---------------------------------------------------------------------------
-template <typename DT, int DP>
+template <typename DT, int DP, bool kWin>
 __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volatile uint32_t* abort_flag) {
   using Tr = DTypeTraits<DT>;
   constexpr uint32_t idesc_qk = umma_idesc_f16(Tr::kBF16, kTileM, kBlockN, false);
@@ -273,18 +296,27 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   const uint32_t v_lo0 = smem_desc_sw128_lo(smem_u32(sm.v[0]), 16384);
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, p_cnt[2] = {0, 0};
 
-  auto fetch = [&](WsUnit& x) -> bool {
+  auto fetch = [&](MmaUnit& x) -> bool {
     const int slot = it_cnt & 1;
     if (!WS_WAIT(&sm.item_full[slot], (it_cnt >> 1) & 1)) return false;
-    x = sm.items[slot];
+    const WsUnit& w = sm.items[slot];
+    x.valid = w.valid;
+    x.paired = w.paired;
+    x.jb = kWin ? w.jb : 0;
+    x.n_all = w.n_all;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      x.j0[t] = kWin ? w.t[t].j0 : 0;
+      x.n[t] = w.t[t].n;
+    }
     mbar_arrive(&sm.item_empty[slot]);
     ++it_cnt;
     return true;
   };
   // Paired unit: S_t = Q_t K_t^T on tile t's own K stage (kv_base: the unit's
   // first K/V load); the K stage is released once the MMA completes.
-  auto pair_s = [&](const WsUnit& x, int t, uint32_t q_lo0, uint32_t kv_base) -> bool {
-    const uint32_t c = kv_base + ((t == 1 && x.t[0].n > 0) ? 1u : 0u);
+  auto pair_s = [&](const MmaUnit& x, int t, uint32_t q_lo0, uint32_t kv_base) -> bool {
+    const uint32_t c = kv_base + ((t == 1 && x.n[0] > 0) ? 1u : 0u);
     const int st = c % kWsStages;
     if (!WS_WAIT(&sm.k_full[st], (c / kWsStages) & 1)) return false;
     tc_fence_after();
@@ -294,7 +326,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     return true;
   };
 
-  WsUnit u;
+  MmaUnit u;
   bool s_issued = false;   // S MMAs of the paired unit u already issued (ahead of u)
   if (!fetch(u)) u.valid = 0;
   while (u.valid) {
@@ -305,7 +337,8 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     }
     if (!u.paired) {
       // ---- one long-sequence block: both tiles share every K/V tile ----
-      const int n = u.n_all;
+      // KV tiles jb .. jb + n - 1 are ring positions kv_cnt ..; tile t visits [j0_t, n_t).
+      const int n = u.n_all, jb = u.jb;
       const int qs = q_cnt % kQSlots;
       if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
       ++q_cnt;
@@ -316,7 +349,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         const uint32_t ks = k_lo0 + (kv_cnt % kWsStages) * kStep;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (u.t[t].n > 0) {
+          if (u.n[t] > 0 && u.j0[t] == jb) {
             issue_qk<DP>(tS[t], q_lo0 + t * kStep, ks, idesc_qk);
             umma_commit(&sm.s_full[t]);
           }
@@ -325,32 +358,34 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         if (n == 1) umma_commit(&sm.q_empty[qs]);
       }
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        const uint32_t c = kv_cnt + j, cn = c + 1;
+      for (int i = 0; i < n && ok; ++i) {
+        const int j = jb + i;
+        const uint32_t c = kv_cnt + i, cn = c + 1;
         const int st = c % kWsStages, stn = cn % kWsStages;
         if (!WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
         const uint32_t vs = v_lo0 + st * kStep;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j >= u.t[t].n) continue;
-          const uint32_t par = p_cnt[t] & 1;
-          ++p_cnt[t];
-          if (!WS_WAIT(&sm.p_lo[t], par)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, j > 0);
-          if (!WS_WAIT(&sm.p_hi[t], par)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
-          umma_commit(&sm.o_full[t]);
-          if (j + 1 < u.t[t].n) {
+          if (j >= u.j0[t] && j < u.n[t]) {
+            const uint32_t par = p_cnt[t] & 1;
+            ++p_cnt[t];
+            if (!WS_WAIT(&sm.p_lo[t], par)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, j > u.j0[t]);
+            if (!WS_WAIT(&sm.p_hi[t], par)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
+            umma_commit(&sm.o_full[t]);
+          }
+          if (j + 1 >= u.j0[t] && j + 1 < u.n[t]) {   // the tile's next S (or its first)
             if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
             tc_fence_after();
             issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + stn * kStep, idesc_qk);
             umma_commit(&sm.s_full[t]);
           }
         }
-        if (j + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
-        if (j == n - 2) umma_commit(&sm.q_empty[qs]);    // last S MMAs of the item issued
+        if (i + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
+        if (i == n - 2) umma_commit(&sm.q_empty[qs]);    // last S MMAs of the item issued
         umma_commit(&sm.v_empty[st]);
       }
       kv_cnt += n;
@@ -368,12 +403,12 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
       ++q_cnt;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
-        if (ok && u.t[t].n > 0) ok = pair_s(u, t, q_lo00 + qs * 2 * kStep, kv_cnt);
+        if (ok && u.n[t] > 0) ok = pair_s(u, t, q_lo00 + qs * 2 * kStep, kv_cnt);
       if (!ok) break;
       umma_commit(&sm.q_empty[qs]);
     }
     // the next unit, if paired, gets its S_t issued right after this unit's P_t V
-    WsUnit nx;
+    MmaUnit nx;
     if (!fetch(nx)) break;
     const bool ahead = nx.valid && nx.paired && nx.n_all > 0;
     const uint32_t kv_next = kv_cnt + u.n_all;
@@ -389,14 +424,14 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     uint32_t par[2], vpar[2], kpar_nx[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const bool s_next = ahead && nx.t[t].n > 0;
-      state[t] = u.t[t].n > 0 ? 1 : (s_next ? 3 : 0);
-      const uint32_t c = kv_cnt + ((t == 1 && u.t[0].n > 0) ? 1u : 0u);
+      const bool s_next = ahead && nx.n[t] > 0;
+      state[t] = u.n[t] > 0 ? 1 : (s_next ? 3 : 0);
+      const uint32_t c = kv_cnt + ((t == 1 && u.n[0] > 0) ? 1u : 0u);
       st[t] = c % kWsStages;
       vpar[t] = (c / kWsStages) & 1;
       par[t] = p_cnt[t] & 1;
-      if (u.t[t].n > 0) ++p_cnt[t];
-      const uint32_t cn = kv_next + ((t == 1 && nx.t[0].n > 0) ? 1u : 0u);
+      if (u.n[t] > 0) ++p_cnt[t];
+      const uint32_t cn = kv_next + ((t == 1 && nx.n[0] > 0) ? 1u : 0u);
       st_nx[t] = cn % kWsStages;
       kpar_nx[t] = (cn / kWsStages) & 1;
     }
@@ -417,7 +452,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
           issue_pv<4, 8>(tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, true);
           umma_commit(&sm.o_full[t]);
           umma_commit(&sm.v_empty[st[t]]);
-          state[t] = (ahead && nx.t[t].n > 0) ? 3 : 0;
+          state[t] = (ahead && nx.n[t] > 0) ? 3 : 0;
           progressed = true;
         }
         if (state[t] == 3) {
@@ -459,7 +494,8 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
 }
 
 // P for 32 keys of one row: exp2(S * scale_log2 - mb), rounded to the input
-// type and packed in pairs, with the rounded and the exact running sums.
+// type and packed in pairs, with the rounded and the exact running sums (two
+// accumulator pairs each, alternating, for two independent add chains).
 template <typename DT>
 __device__ __forceinline__ void ws_exp_chunk(const uint32_t* sr, uint32_t* pk, float2 scale2, float2 bias2, float2& lr_a,
                                              float2& lr_b, float2& le_a, float2& le_b) {
@@ -481,24 +517,21 @@ __device__ __forceinline__ void ws_exp_chunk(const uint32_t* sr, uint32_t* pk, f
   }
 }
 
-// Last visible column of KV tile j (keys from kv0) for query position qpos
-// (negative: none; rows past the sequence see none).
-__device__ __forceinline__ int ws_row_lim(const SeqInfo& s, int qpos, bool row_valid, int kv0) {
-  return row_valid ? (s.causal ? min(s.kv_len - 1, qpos + s.shift) : s.kv_len - 1) - kv0 : -1;
-}
-
 // Softmax of one KV tile for one row (the calling thread's TMEM lane): S from
 // TMEM, online max / sums, P (rounded to the input type) back over S in two
-// halves of 64 keys, lazy O rescale.  `partial` (tile-uniform): some row of
-// the tile may not see all 128 keys; columns past the row's last visible key
+// halves of 64 keys, lazy O rescale.  `partial` (warp-uniform): some row of
+// the warp may not see all 128 keys; columns outside the row's visible keys
 // are masked, and when no row of the warp sees a key in the second half, its
-// exponentials are skipped and zero P is stored there.
-// Returns false when a wait gave up.
-template <typename DT, int DP>
+// exponentials are skipped and zero P is stored there.  j: position of the KV
+// tile among the tiles this Q tile visits (row_first / row_last are counted
+// from the first of them).  Returns false when a wait gave up.
+// row_first / row_last: the row's first and last visible key (row_last < 0 for
+// rows past the sequence); kWin: a window may bound the keys from below.
+template <typename DT, int DP, bool kWin>
 __device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams& p, volatile uint32_t* abort_flag,
-                                                uint32_t tS, uint32_t tO, int tile, int j, uint32_t o_cnt, bool partial,
-                                                const SeqInfo& s, int qpos, bool row_valid, float sl2, float& m_run,
-                                                float2& lr_a, float2& lr_b, float2& le_a, float2& le_b) {
+                                                uint32_t tS, uint32_t tO, int tile, int j, uint32_t o_cnt,
+                                                bool partial, int row_first, int row_last, float sl2,
+                                                float& m_run, float2& lr_a, float2& lr_b, float2& le_a, float2& le_b) {
   const int lane = threadIdx.x & 31;
   const int kv0 = j * kBlockN;
   uint32_t sr[128];
@@ -509,10 +542,17 @@ __device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams
   tmem_tie_regs32(sr + 64);
   tmem_tie_regs32(sr + 96);
   if (partial) {
-    const int lim = ws_row_lim(s, qpos, row_valid, kv0);
+    const int lim = row_last - kv0;
+    if constexpr (kWin) {   // sliding window: keys before the row's window too
+      const int lo = row_first - kv0;
 #pragma unroll
-    for (int c = 0; c < 128; ++c)
-      if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+      for (int c = 0; c < 128; ++c)
+        if (c > lim || c < lo) sr[c] = __float_as_uint(-INFINITY);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+    }
   }
   // row max: three-input max, four independent chains
   float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -542,7 +582,7 @@ __device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     if (partial && half == 1 &&
-        __all_sync(0xffffffffu, ws_row_lim(s, qpos, row_valid, kv0) < 2 * 32)) {
+        __all_sync(0xffffffffu, row_last - kv0 < 2 * 32)) {
       // no row of the warp sees keys 64..127: their P is zero
       uint32_t pk[16];
 #pragma unroll
@@ -583,7 +623,7 @@ __device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams
 // ---------------------------------------------------------------------------
 // warps 2-9: softmax + epilogue, tile = (warp - 2) / 4
 // ---------------------------------------------------------------------------
-template <typename DT, int DP>
+template <typename DT, int DP, bool kWin>
 __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, int tile,
                            volatile uint32_t* abort_flag) {
   using Tr = DTypeTraits<DT>;
@@ -615,20 +655,27 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
     float2 lr_a = make_float2(0.f, 0.f), lr_b = lr_a;   // rounded-P sums (normalise O)
     float2 le_a = lr_a, le_b = lr_a;                     // exact sums (LSE)
     bool ok = true;
-    for (int j = 0; j < ni; ++j) {
+    // the row's visible keys (none for rows past the sequence), counted from the
+    // first KV tile the Q tile visits; the loop runs over the nv tiles it visits
+    const int base = kWin ? tt.j0 * kBlockN : 0;
+    const int row_last = row < rows ? seq_last_key(s, qpos) - base : -1;
+    const int row_first = kWin ? seq_first_key(s, qpos) - base : 0;
+    const int tile_last = seq_last_key(s, qt0) - base;   // smallest last key of the tile's rows
+    const int nv = ni - (kWin ? tt.j0 : 0);
+    for (int j = 0; j < nv; ++j) {
       if (!WS_WAIT_WARP(&sm.s_full[tile], s_cnt & 1)) { ok = false; break; }
       ++s_cnt;
       tc_fence_after();
-      // partial tile: the sequence ends inside it, or it crosses the causal diagonal
+      // partial tile: a row's visible keys end (sequence end, causal diagonal,
+      // window) inside it, or (window) start inside it for a row of this warp
       const int kv0 = j * kBlockN;
-      const bool masked = kv0 + kBlockN > s.kv_len || (s.causal && kv0 + kBlockN - 1 > qt0 + s.shift);
-
-      ok = ws_softmax_tile<DT, DP>(sm, p, abort_flag, tS, tO, tile, j, o_cnt, masked, s, qpos, row < rows, sl2, m_run,
-                                   lr_a, lr_b, le_a, le_b);
+      const bool masked = kv0 + kBlockN - 1 > tile_last || (kWin && __any_sync(0xffffffffu, row_first > kv0));
+      ok = ws_softmax_tile<DT, DP, kWin>(sm, p, abort_flag, tS, tO, tile, j, o_cnt, masked, row_first, row_last, sl2,
+                                         m_run, lr_a, lr_b, le_a, le_b);
       if (!ok) break;
     }
     if (!ok) break;
-    o_cnt += ni;
+    o_cnt += nv;
 
     // ---- epilogue ----
     const bool row_ok = row < rows;
@@ -666,7 +713,7 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
   }
 }
 
-template <typename DT, int DP>
+template <typename DT, int DP, bool kWin>
 __global__ void __launch_bounds__(kWsThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -713,13 +760,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   volatile uint32_t* abort_flag = &sm.abort;
 
   if (warp == 0) {
-    ws_producer<DP>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
+    ws_producer<DP, kWin>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) ws_mma<DT, DP>(sm, p, tmem, abort_flag);
+    if (lane == 0) ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
     __syncwarp();
   } else {
     zero_pad_rows(p, 64, kWsThreads - 64, 2);
-    ws_softmax<DT, DP>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
+    ws_softmax<DT, DP, kWin>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
   }
 
   tc_fence_before();

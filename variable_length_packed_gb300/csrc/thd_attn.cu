@@ -102,7 +102,9 @@ size_t one_cta_per_sm(size_t bytes) { return bytes > kOneCtaPerSmSmem ? bytes : 
 template <typename DT, int DP>
 int launch_ws(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const thd::AttnParams& p,
               int grid, cudaStream_t stream) {
-  auto kern = thd::attn_fwd_ws_kernel<DT, DP>;
+  // the windowed instantiation carries the window's lower bound through the pipeline
+  const bool win = p.win_left >= 0 || p.win_right >= 0;
+  auto kern = win ? thd::attn_fwd_ws_kernel<DT, DP, true> : thd::attn_fwd_ws_kernel<DT, DP, false>;
   const size_t smem = one_cta_per_sm(sizeof(thd::WsSmem<DP>) + 1024);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return THD_ERR_CUDA;
@@ -141,13 +143,15 @@ size_t thd_attn_bwd_workspace_size(int total_tokens, int num_heads_q, int head_d
   return bwd_workspace_bytes(total_tokens, num_heads_q, head_dim);
 }
 
-int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
-                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
-                 const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size, int max_seqlen,
-                 float softmax_scale, void* dq, void* dk, void* dv, int total_tokens, int num_heads_q,
-                 int num_heads_kv, int head_dim, int dtype, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+int thd_attn_bwd_window(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                        const void* dout, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                        const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                        const uint8_t* seq_is_causal, int batch_size, int max_seqlen, float softmax_scale, void* dq,
+                        void* dk, void* dv, int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                        int dtype, int window_left, int window_right, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   if (batch_size < 0 || max_seqlen < 0 || total_tokens < 0) return THD_ERR_ARG;
+  if (window_left < -1 || window_right < -1) return THD_ERR_ARG;
   if (num_heads_q < 1 || num_heads_kv < 1) return THD_ERR_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return THD_ERR_ARG;
   if (dtype != THD_BF16 && dtype != THD_FP16) return THD_ERR_UNSUPPORTED;
@@ -195,6 +199,8 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
   p.Hq = num_heads_q;
   p.Hkv = num_heads_kv;
   p.d = head_dim;
+  p.win_left = window_left;
+  p.win_right = window_right;
   p.group = num_heads_q / num_heads_kv;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -220,6 +226,18 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
   }
   if (head_dim == 128) return launch_bwd<__half, 128>(mq, mk, mv, mdo, bp, sms, st);
   return launch_bwd<__half, 64>(mq, mk, mv, mdo, bp, sms, st);
+}
+
+int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size, int max_seqlen,
+                 float softmax_scale, void* dq, void* dk, void* dv, int total_tokens, int num_heads_q,
+                 int num_heads_kv, int head_dim, int dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return thd_attn_bwd_window(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                             cu_seqlens_kv_padded, seq_is_causal, batch_size, max_seqlen, softmax_scale, dq, dk, dv,
+                             total_tokens, num_heads_q, num_heads_kv, head_dim, dtype, -1, -1, workspace,
+                             workspace_bytes, stream);
 }
 
 
@@ -277,14 +295,15 @@ int thd_attn_merge(const void* out_a, const float* lse_a, const void* out_b, con
   return e == cudaSuccess ? THD_OK : THD_ERR_CUDA;
 }
 
-int thd_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
-                 const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size,
-                 int max_seqlen, float softmax_scale, void* out, float* lse, int total_tokens, int num_heads_q,
-                 int num_heads_kv, int head_dim, int dtype, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+int thd_attn_fwd_window(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                        const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                        const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size,
+                        int max_seqlen, float softmax_scale, void* out, float* lse, int total_tokens,
+                        int num_heads_q, int num_heads_kv, int head_dim, int dtype, int window_left,
+                        int window_right, void* workspace, size_t workspace_bytes, void* stream) {
   // ---- host-checkable arguments ----
   if (batch_size < 0 || max_seqlen < 0 || total_tokens < 0) return THD_ERR_ARG;
+  if (window_left < -1 || window_right < -1) return THD_ERR_ARG;
   if (num_heads_q < 1 || num_heads_kv < 1) return THD_ERR_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return THD_ERR_ARG;
   if (dtype != THD_BF16 && dtype != THD_FP16) return THD_ERR_UNSUPPORTED;
@@ -329,6 +348,8 @@ int thd_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_
   p.Hq = num_heads_q;
   p.Hkv = num_heads_kv;
   p.d = head_dim;
+  p.win_left = window_left;
+  p.win_right = window_right;
   p.group = num_heads_q / num_heads_kv;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -360,6 +381,17 @@ int thd_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_
     if (head_dim < 64) return launch_serial<__half, 64, false>(mq, mk, mv, p, grid, st);
     return launch_serial<__half, 128, false>(mq, mk, mv, p, grid, st);
   }
+}
+
+int thd_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, const uint8_t* seq_is_causal, int batch_size,
+                 int max_seqlen, float softmax_scale, void* out, float* lse, int total_tokens, int num_heads_q,
+                 int num_heads_kv, int head_dim, int dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return thd_attn_fwd_window(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                             seq_is_causal, batch_size, max_seqlen, softmax_scale, out, lse, total_tokens,
+                             num_heads_q, num_heads_kv, head_dim, dtype, -1, -1, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
