@@ -53,6 +53,20 @@ def effective_flops(w):
     return 4.0 * w.head_dim * w.num_heads_q * pairs
 
 
+def window_pairs(w, left, right):
+    """Visible (query, key) pairs of a self-attention batch under a sliding window: query i of a
+    sequence sees keys max(0, i - left) .. min(L - 1, i + right) (right 0 for causal sequences),
+    the band of thd_attn_fwd_window with shift 0."""
+    pairs = 0
+    for L, c in zip(w.lengths, w.causal):
+        i = np.arange(int(L), dtype=np.int64)
+        lo = np.maximum(0, i - left) if left >= 0 else np.zeros_like(i)
+        r = 0 if c else right
+        hi = np.minimum(int(L) - 1, i + r) if r >= 0 else np.full_like(i, int(L) - 1)
+        pairs += int(np.maximum(hi - lo + 1, 0).sum())
+    return float(pairs)
+
+
 def attn_bytes(w):
     """Algorithmic HBM bytes of one attention launch: Q, K, V read once, O and LSE written once."""
     T, e = w.total_tokens, 2
@@ -380,6 +394,36 @@ def run_gpu(args, ws, rank, local):
                         "heads_kv": ow.num_heads_kv, "head_dim": ow.head_dim, "dtype": str(ow.dtype)}
         del oq, ok_, ov, oout, olse
 
+    # ---- sliding window (local attention, +-2048 keys around the diagonal) on the same batch ----
+    window = None
+    if not args.attn_only and not args.no_window:
+        left = right = 2048
+        wout = torch.empty_like(q)
+        wlse = torch.empty_like(lse)
+
+        def wcall():
+            vlp.thd_attn_fwd(q, k, v, cu, cu, None, None, causal, w.batch_size, S, w.softmax_scale, out=wout,
+                             lse=wlse, workspace=wsp, window=(left, right))
+        for _ in range(3):
+            wcall()
+        torch.cuda.synchronize()
+        wst = int(wsp[8:12].cpu().numpy().view(np.uint32)[0])
+        reps = 10
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for _ in range(reps):
+            wcall()
+        w1.record(stream)
+        torch.cuda.synchronize()
+        wms = w0.elapsed_time(w1) / reps
+        weff = 4.0 * w.head_dim * w.num_heads_q * window_pairs(w, left, right)
+        window = {"window": [left, right], "workload": args.workload, "ms_per_launch": wms,
+                  "effective_tflops": weff / (wms * 1e-3) / 1e12,
+                  "frac_of_bf16_peak": weff / (wms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                  "flops_counted": "4 * d * Hq per visible (query, key) pair in the band",
+                  "device_status_word": wst}
+        del wout, wlse
+
     # ---- padding mask alone on the 4096 x 8192 workload (CUDA graph of back-to-back launches) ----
     mw = workloads.make_mask()
     mcu = torch.from_numpy(mw.cu_seqlens).to(dev)
@@ -496,6 +540,7 @@ def run_gpu(args, ws, rank, local):
                 "pipelining": "two buffer sets; step i+1's H2D and step i-1's D2H overlap step i's kernels"},
         "other_workloads": others,
         "backward": backward,
+        "sliding_window": window,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.result,
         "device_status_word": status,
@@ -524,6 +569,7 @@ def main():
     ap.add_argument("--also", nargs="*", default=["padded_gaps", "mixed_gqa", "many_short"],
                     help="other packed batches whose attention launch is timed alone (after the step)")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
+    ap.add_argument("--no-window", action="store_true", help="skip timing the sliding-window forward")
     ap.add_argument("--attn-only", action="store_true",
                     help="run only the attention launches (warm-up + timed) and print the line; "
                          "for profiler captures")

@@ -21,6 +21,18 @@ def test_effective_flops_counts_unmasked_pairs():
     assert bench.effective_flops(w) == 4 * 16 * 3 * pairs
 
 
+def test_window_pairs_match_the_oracle_band():
+    import oracle
+    w = workloads.from_lengths("wp", [1, 37, 300, 129], [1, 0, 1, 0], heads_q=2, head_dim=16, seed=0)
+    for left, right in ((-1, -1), (5, 0), (0, 0), (64, 64), (-1, 3), (1000, 7)):
+        ref = 0
+        for L, c in zip(w.lengths, w.causal):
+            for i in range(int(L)):
+                lo, hi = oracle.visible_range(i, int(L), int(L), 1 if c else 0, (left, right))
+                ref += hi - lo
+        assert bench.window_pairs(w, left, right) == ref, (left, right)
+
+
 def test_attn_bytes_formula():
     w = workloads.from_lengths("b", [4, 6], [1, 0], heads_q=4, heads_kv=2, head_dim=8, seed=0)
     T = w.total_tokens
