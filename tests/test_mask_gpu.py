@@ -45,7 +45,8 @@ def test_large_workload_bit_exact():
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("B,S,offset", [(3, 5, 1), (7, 33, 3), (5, 16, 0), (9, 17, 15), (1, 1, 7), (64, 100, 9)])
+@pytest.mark.parametrize("B,S,offset", [(3, 5, 1), (7, 33, 3), (5, 16, 0), (9, 17, 15), (1, 1, 7), (64, 100, 9),
+                                         (33, 48, 0), (130, 256, 0), (3, 8192, 0), (2000, 32, 0), (11, 64, 4)])
 def test_shapes_and_alignment(B, S, offset):
     rng = np.random.default_rng(B * 100 + S)
     lens = rng.integers(0, S + 3, size=B)             # includes rows longer than S
@@ -58,8 +59,9 @@ def test_shapes_and_alignment(B, S, offset):
 
 def test_non_monotone_and_returned_tensor():
     cu = np.array([10, 3, 3, 40, 2], dtype=np.int32)   # negative and oversized lengths
-    got = gpu_mask(cu, 4, 12)
-    assert np.array_equal(got, oracle.padding_mask_formula(cu, 4, 12).astype(np.uint8))
+    for S in (12, 32):                                 # flat and row-per-warp paths
+        got = gpu_mask(cu, 4, S)
+        assert np.array_equal(got, oracle.padding_mask_formula(cu, 4, S).astype(np.uint8))
     m = vlp.thd_padding_mask(torch.tensor([0, 2, 5], dtype=torch.int32, device="cuda"), 2, 4)
     assert m.dtype == torch.bool and m.shape == (2, 1, 1, 4)
     assert m.cpu().numpy().reshape(2, 4).tolist() == [[False, False, True, True], [False, False, False, True]]

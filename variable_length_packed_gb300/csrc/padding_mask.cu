@@ -6,14 +6,18 @@
 // 0..B of cu are read (Changes: longer buffers are allowed), and a sequence
 // longer than S gives an all-False row (Equivalence).
 //
-// The output is a pure HBM write stream.  Each thread writes whole 16-byte
-// chunks of the flat B*S byte array (a warp store covers 512 contiguous
-// bytes).  Within one row the mask bytes of a chunk form a step (0 ... 0 1 ... 1),
-// so a chunk is built from at most two steps with 64-bit shifts instead of 16
-// compares.  The chunk's row is found with one exact division by the invariant
-// S: a multiply-high by a reciprocal precomputed on the host (division by
-// invariant integers using multiplication, Granlund & Montgomery, 1994).  The
-// unaligned head and tail bytes of the buffer are written one at a time.
+// The output is a pure HBM write stream, written in 16-byte chunks (a warp
+// store covers 512 contiguous bytes).  Within one row the mask bytes of a chunk
+// form a step (0 ... 0 1 ... 1), built with 64-bit shifts instead of 16
+// compares.
+//  * Rows of whole, aligned chunks (S a multiple of 16, 16-byte aligned mask):
+//    a warp writes one row at a time, its length read once; no division.
+//  * Otherwise the flat B*S array is cut into chunks regardless of rows; a chunk
+//    spans at most two rows, and its row is found with one exact division by the
+//    invariant S: a multiply-high by a reciprocal precomputed on the host
+//    (division by invariant integers using multiplication, Granlund &
+//    Montgomery, 1994).  The unaligned head and tail bytes are written one at a
+//    time.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -119,6 +123,24 @@ __global__ void __launch_bounds__(256) padding_mask_kernel(const MaskArgs a) {
   }
 }
 
+// Row path: S = 16 * chunks_per_row, mask 16-byte aligned.  Warp w writes rows
+// w, w + warps, ...; lane l writes chunks l, l + 32, ... of the row.
+__global__ void __launch_bounds__(256) padding_mask_rows_kernel(const int32_t* cu, uint8_t* mask, int B,
+                                                                int chunks_per_row) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < B; b += warps) {
+    const long long len = row_len(cu, b);
+    uint4* row = reinterpret_cast<uint4*>(mask + (size_t)b * (size_t)chunks_per_row * 16u);
+#pragma unroll 4
+    for (int k = lane; k < chunks_per_row; k += 32) {
+      uint64_t lo, hi;
+      step_from(clampi(len - 16ll * k, 0, 16), lo, hi);
+      row[k] = make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+    }
+  }
+}
+
 }  // namespace
 
 // Host launcher (called from the C ABI in thd_attn.cu after validation).
@@ -135,10 +157,16 @@ cudaError_t launch_padding_mask(const int32_t* cu, int B, int S, uint8_t* mask, 
   a.div32 = a.total <= 0xFFFFFFFFll ? 1 : 0;
   a.recip = S > 1 ? (0xFFFFFFFFFFFFFFFFull / (uint64_t)S) + 1ull : 0ull;
   const int threads = 256;
+  const long long cap_blocks = (long long)num_sms * 8;   // 8 resident 256-thread blocks per SM
+  if (S % 16 == 0 && a.head == 0 && B > 0) {
+    const long long rows_blocks = ((long long)B + 7) / 8;   // one row per warp
+    const int grid = (int)(rows_blocks < cap_blocks ? rows_blocks : cap_blocks);
+    padding_mask_rows_kernel<<<grid, threads, 0, stream>>>(cu, mask, B, S / 16);
+    return cudaGetLastError();
+  }
   long long want = (a.nchunks + 4 * threads - 1) / (4 * threads);
   if (want < 1) want = 1;
-  const long long cap = (long long)num_sms * 8;   // 8 resident 256-thread blocks per SM
-  const int grid = (int)(want < cap ? want : cap);
+  const int grid = (int)(want < cap_blocks ? want : cap_blocks);
   padding_mask_kernel<<<grid, threads, 0, stream>>>(a);
   return cudaGetLastError();
 }
