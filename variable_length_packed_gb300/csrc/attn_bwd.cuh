@@ -21,8 +21,10 @@
 //         dK / dV accumulate in TMEM and are written once per item; dQ tiles
 //         are added to the fp32 accumulator with vector atomics.
 //   post  dQ = scale * accumulator, rounded to the input type.
-// head_dim 64 or 128 (TMA loads).  Each step waits for the previous one
-// (correctness-first structure, four warps).
+// head_dim 64 or 128 (TMA loads).  Eight warps: warps w and w + 4 read the
+// same TMEM lanes and split the columns of the elementwise step, the dQ
+// atomics and the dK / dV epilogue; the next query tile's Q and dO load while
+// the current tile's dQ is added.
 #pragma once
 #include "attn_common.cuh"
 
@@ -141,8 +143,10 @@ struct BwdSmem {
   SchedSmem sched;
 };
 
+constexpr int kBwdThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lanes, split the columns
+
 template <typename DT, int DP>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams bp) {
@@ -152,12 +156,15 @@ __global__ void __launch_bounds__(128, 1)
   BwdSmem<DP>& sm = *reinterpret_cast<BwdSmem<DP>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & (kTileM - 1);    // TMEM lane: key row of the tile (query row for dQ)
+  const int half = tid >> 7;             // column half handled by this thread
   constexpr int kPanels = DP / 64;
   constexpr uint32_t kTileBytes = BwdSmem<DP>::kTileBytes;
   constexpr uint32_t idesc_s = umma_idesc_f16(Tr::kBF16, kTileM, kTileM, false);   // S^T, dP^T
   constexpr uint32_t idesc_acc = umma_idesc_f16(Tr::kBF16, kTileM, DP, true);      // dV, dK (A in TMEM)
   constexpr uint32_t idesc_dq = umma_idesc_f16_ab(Tr::kBF16, kTileM, DP, true, true);
   constexpr uint32_t hi = smem_desc_sw128_hi(1024);
+  constexpr int kHalfChunks = DP / 64;   // 32-column chunks of a head_dim-wide row per half
 
   if (tid == 0) {
     mbar_init(&sm.bar_kv, 1);
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
+  const uint32_t t_lane = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t tDK = tmem, tDV = tmem + DP, tS = tmem + 256, tDP = tmem + 384;
   // low descriptor words: K-major use (head_dim contracted) and MN-major use (rows contracted)
   const uint32_t k_K = smem_desc_sw128_lo(smem_u32(sm.k), 16), k_MN = smem_desc_sw128_lo(smem_u32(sm.k), 16384);
@@ -191,6 +198,18 @@ __global__ void __launch_bounds__(128, 1)
   const float sl2 = p.scale_log2;
   volatile uint32_t* abort_flag = &sm.abort;
   uint32_t ph_kv = 0, ph_q = 0, ph_mma = 0;
+  bool q_in_flight = false;   // thread 0: a Q / dO load not yet waited for
+
+  // thread 0: Q and dO rows q_start + q0 .. of query head h into shared memory
+  auto load_q = [&](int h, int q_row) {
+    mbar_arrive_expect_tx(&sm.bar_q, 2 * kTileBytes);
+#pragma unroll
+    for (int pn = 0; pn < kPanels; ++pn) {
+      tma_load_2d(sm.q + pn * 16384, &tm_q, &sm.bar_q, h * p.d + pn * 64, q_row);
+      tma_load_2d(sm.dout + pn * 16384, &tm_do, &sm.bar_q, h * p.d + pn * 64, q_row);
+    }
+    q_in_flight = true;
+  };
 
   Claimer claimer{0ull, 0};   // used by warp 0
   for (;;) {
@@ -205,7 +224,7 @@ __global__ void __launch_bounds__(128, 1)
     const SeqInfo& s = it.seq;
     const int g = it.h, kv0 = it.qblock * kTileM;
     const int keys_valid = min(kTileM, s.kv_len - kv0);
-    const int key = kv0 + tid;                       // this thread's key position (TMEM lane)
+    const int key = kv0 + row;                       // this thread's key position (TMEM lane)
     // query tiles holding a query that sees a key of [kv0, kv0 + 128): query i sees key j
     // only if i + shift - lo_off <= j <= i + shift + hi_off
     const long long first_q = (long long)kv0 - s.shift - s.hi_off;
@@ -221,6 +240,7 @@ __global__ void __launch_bounds__(128, 1)
         tma_load_2d(sm.k + pn * 16384, &tm_k, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
         tma_load_2d(sm.v + pn * 16384, &tm_v, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
       }
+      load_q(g * p.group, s.q_start + qt_first * kTileM);   // the item's first query tile
     }
     bool first = true;
     bool stop = false;
@@ -229,27 +249,22 @@ __global__ void __launch_bounds__(128, 1)
       for (int qt = qt_first; qt < nqt; ++qt) {
         const int q0 = qt * kTileM;
         const int rows_q = min(kTileM, s.q_len - q0);
-        if (tid == 0) {
-          mbar_arrive_expect_tx(&sm.bar_q, 2 * kTileBytes);
-#pragma unroll
-          for (int pn = 0; pn < kPanels; ++pn) {
-            tma_load_2d(sm.q + pn * 16384, &tm_q, &sm.bar_q, h * p.d + pn * 64, s.q_start + q0);
-            tma_load_2d(sm.dout + pn * 16384, &tm_do, &sm.bar_q, h * p.d + pn * 64, s.q_start + q0);
+        if (tid < kTileM) {
+          if (tid < rows_q) {
+            const size_t li = (size_t)h * p.T + s.q_start + q0 + tid;
+            sm.lse2[tid] = p.lse[li] * 1.4426950408889634f;
+            sm.dd[tid] = bp.D[li];
+          } else {
+            sm.lse2[tid] = 0.f;
+            sm.dd[tid] = 0.f;
           }
-        }
-        if (tid < rows_q) {
-          const size_t li = (size_t)h * p.T + s.q_start + q0 + tid;
-          sm.lse2[tid] = p.lse[li] * 1.4426950408889634f;
-          sm.dd[tid] = bp.D[li];
-        } else {
-          sm.lse2[tid] = 0.f;
-          sm.dd[tid] = 0.f;
         }
         __syncthreads();
         // ---- S^T = K Q^T, dP^T = V dO^T ----
         if (tid == 0) {
           if (first) mbar_wait(&sm.bar_kv, ph_kv, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
           mbar_wait(&sm.bar_q, ph_q, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
+          q_in_flight = false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
@@ -269,7 +284,7 @@ __global__ void __launch_bounds__(128, 1)
         ph_mma ^= 1u;
         tc_fence_after();
 
-        // ---- P^T and dS^T for this thread's key row, 32 queries at a time ----
+        // ---- P^T and dS^T for this thread's key row and column half ----
         // query column c of the tile sees this key iff c_lo <= c <= c_hi (query
         // q0 + c sees key j iff j - shift - hi_off <= q0 + c <= j - shift + lo_off)
         const bool kvalid = key < s.kv_len;
@@ -277,7 +292,8 @@ __global__ void __launch_bounds__(128, 1)
         const int c_lo = (int)min(max(kd - s.hi_off, -1ll), (long long)kTileM);
         const int c_hi = (int)max(min(kd + s.lo_off, (long long)rows_q - 1), -1ll);
 #pragma unroll
-        for (int c0 = 0; c0 < 4; ++c0) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c0 = 2 * half + cc;   // 32-column chunk
           uint32_t sr[32], dr[32];
           tmem_ld32(tS + t_lane + 32 * c0, sr);
           tmem_ld32(tDP + t_lane + 32 * c0, dr);
@@ -298,11 +314,13 @@ __global__ void __launch_bounds__(128, 1)
             pp[e] = Tr::pack2(pv[0], pv[1]);
             pd[e] = Tr::pack2(dsv[0], dsv[1]);
           }
-          tmem_st16(tS + t_lane + 16 * c0, pp);     // P^T over S^T columns already read
-          tmem_st16(tDP + t_lane + 16 * c0, pd);    // dS^T over dP^T columns already read
+          // P^T / dS^T of these 32 queries over the first 16 of their own 32 S^T / dP^T
+          // columns: the other column half may still be reading its chunks
+          tmem_st16(tS + t_lane + 32 * c0, pp);
+          tmem_st16(tDP + t_lane + 32 * c0, pd);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4*>(sm.ds + sw128_offset(tid, 4 * c0 + e)) =
+            *reinterpret_cast<uint4*>(sm.ds + sw128_offset(row, 4 * c0 + e)) =
                 make_uint4(pd[4 * e], pd[4 * e + 1], pd[4 * e + 2], pd[4 * e + 3]);
         }
         tmem_st_wait();
@@ -313,12 +331,15 @@ __global__ void __launch_bounds__(128, 1)
         // ---- dV += P^T dO, dK += dS^T Q, dQ_tile = dS K ----
         if (tid == 0) {
           tc_fence_after();
+          // 16 queries per step: 8 TMEM columns of P^T / dS^T, two steps per 32-column chunk
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts(tDV, tS + kk * 8, smem_desc_join(o_MN + kk * 128, hi), idesc_acc, (!first || kk > 0) ? 1u : 0u);
+            umma_ts(tDV, tS + 32 * (kk >> 1) + 8 * (kk & 1), smem_desc_join(o_MN + kk * 128, hi), idesc_acc,
+                    (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts(tDK, tDP + kk * 8, smem_desc_join(q_MN + kk * 128, hi), idesc_acc, (!first || kk > 0) ? 1u : 0u);
+            umma_ts(tDK, tDP + 32 * (kk >> 1) + 8 * (kk & 1), smem_desc_join(q_MN + kk * 128, hi), idesc_acc,
+                    (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ss(tS, smem_desc_join(ds_MN + kk * 128, hi), smem_desc_join(k_MN + kk * 128, hi), idesc_dq,
@@ -329,15 +350,22 @@ __global__ void __launch_bounds__(128, 1)
         ph_mma ^= 1u;
         tc_fence_after();
         first = false;
+        // Q and dO are free once these MMAs completed: the next query tile of the
+        // item loads while this tile's dQ goes out
+        if (tid == 0 && !*abort_flag) {
+          if (qt + 1 < nqt) load_q(h, s.q_start + (qt + 1) * kTileM);
+          else if (hh + 1 < p.group) load_q(h + 1, s.q_start + qt_first * kTileM);
+        }
 
-        // ---- dQ rows (this thread = query q0 + tid) into the fp32 accumulator ----
-        float* dst = bp.dacc + ((size_t)(s.q_start + q0 + tid) * p.Hq + h) * (size_t)p.d;
+        // ---- dQ rows (this thread = query q0 + row, one column half) into the fp32 accumulator ----
+        float* dst = bp.dacc + ((size_t)(s.q_start + q0 + row) * p.Hq + h) * (size_t)p.d;
 #pragma unroll
-        for (int c = 0; c < DP / 32; ++c) {
+        for (int cc = 0; cc < kHalfChunks; ++cc) {
+          const int c = half * kHalfChunks + cc;
           uint32_t o[32];
           tmem_ld32(tS + t_lane + 32 * c, o);
           tmem_ld_wait_regs32(o);
-          if (tid < rows_q) {
+          if (row < rows_q) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + e),
@@ -353,15 +381,16 @@ __global__ void __launch_bounds__(128, 1)
       }
     }
 
-    // ---- dK, dV rows of this key tile ----
+    // ---- dK, dV rows of this key tile (one column half per thread) ----
     if (keys_valid > 0) {
-      const bool row_ok = tid < keys_valid;
+      const bool row_ok = row < keys_valid;
       const size_t base = ((size_t)(s.kv_start + (row_ok ? key : kv0)) * p.Hkv + g) * (size_t)p.d;
       DT* dkp = static_cast<DT*>(bp.dk) + base;
       DT* dvp = static_cast<DT*>(bp.dv) + base;
       if (any && !first) {
 #pragma unroll
-        for (int c = 0; c < DP / 32; ++c) {
+        for (int cc = 0; cc < kHalfChunks; ++cc) {
+          const int c = half * kHalfChunks + cc;
           uint32_t a[32], b[32];
           tmem_ld32(tDK + t_lane + 32 * c, a);
           tmem_ld32(tDV + t_lane + 32 * c, b);
@@ -385,7 +414,7 @@ __global__ void __launch_bounds__(128, 1)
           }
         }
       } else if (row_ok) {
-        for (int c = 0; c < DP; c += 8) {
+        for (int c = half * (DP / 2); c < (half + 1) * (DP / 2); c += 8) {
           *reinterpret_cast<uint4*>(dkp + c) = make_uint4(0u, 0u, 0u, 0u);
           *reinterpret_cast<uint4*>(dvp + c) = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -395,6 +424,13 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after();
     if (stop) break;
+  }
+  // a Q / dO load issued ahead lands before the CTA can exit (only after an abort)
+  if (tid == 0 && q_in_flight) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&sm.bar_q, ph_q)) {
+      if (globaltimer_ns() - t0 > 200000000ull) break;
+    }
   }
 
   tc_fence_before();

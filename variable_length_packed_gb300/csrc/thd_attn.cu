@@ -128,7 +128,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const size_t smem = one_cta_per_sm(sizeof(thd::BwdSmem<DP>) + 1024);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return THD_ERR_CUDA;
-  kern<<<sms, 128, smem, stream>>>(mq, mk, mv, mdo, bp);
+  kern<<<sms, thd::kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, bp);
   if (cudaGetLastError() != cudaSuccess) return THD_ERR_CUDA;
   thd::attn_bwd_post_kernel<DT><<<small_grid, 256, 0, stream>>>(bp);
   return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
