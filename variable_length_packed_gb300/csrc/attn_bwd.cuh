@@ -19,7 +19,7 @@
 //            dV += P^T dO, dK += dS^T Q           (A operand from TMEM)
 //            dQ_tile = dS K                       (A = dS^T read MN-major)
 //         dK / dV accumulate in TMEM and are written once per item; dQ tiles
-//         are added to the fp32 accumulator with vector atomics.
+//         are added to the fp32 accumulator by bulk tensor reductions (TMA).
 //   post  dQ = scale * accumulator, rounded to the input type.
 // head_dim 64 or 128 (TMA loads).  Eight warps: warps w and w + 4 read the
 // same TMEM lanes and split the columns of the elementwise step, the dQ
@@ -149,7 +149,7 @@ template <typename DT, int DP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdParams bp) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams bp) {
   using Tr = DTypeTraits<DT>;
   const AttnParams& p = bp.a;
   extern __shared__ uint8_t smem_raw[];
@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   if (warp == 0) {
     tmem_alloc(&sm.tmem_base, 512);
@@ -357,21 +358,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           else if (hh + 1 < p.group) load_q(h + 1, s.q_start + qt_first * kTileM);
         }
 
-        // ---- dQ rows (this thread = query q0 + row, one column half) into the fp32 accumulator ----
-        float* dst = bp.dacc + ((size_t)(s.q_start + q0 + row) * p.Hq + h) * (size_t)p.d;
+        // ---- dQ tile into the fp32 accumulator: 64 columns at a time through the dS^T
+        // buffer (free once the dQ MMA completed) and a bulk tensor reduction ----
 #pragma unroll
-        for (int cc = 0; cc < kHalfChunks; ++cc) {
-          const int c = half * kHalfChunks + cc;
+        for (int r = 0; r < DP / 64; ++r) {
+          const int c = 2 * r + half;   // 32-column chunk: panel `half` of the buffer
           uint32_t o[32];
           tmem_ld32(tS + t_lane + 32 * c, o);
           tmem_ld_wait_regs32(o);
-          if (row < rows_q) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + e),
-                        make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
-                                    __uint_as_float(o[e + 3])));
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(sm.ds + sw128_offset(row, 8 * half + e)) =
+                make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          fence_proxy_async_smem();
+          __syncthreads();
+          if (tid == 0) {
+            // rows past the sequence carry dS = 0, so their (zero) rows add nothing
+            tma_reduce_add_2d(&tm_dq, sm.ds, h * p.d + 64 * r, s.q_start + q0);
+            tma_reduce_add_2d(&tm_dq, sm.ds + 16384, h * p.d + 64 * r + 32, s.q_start + q0);
+            bulk_commit_group();
+            bulk_wait_group_read0();   // the buffer is free again
           }
+          __syncthreads();
         }
         tc_fence_before();
         if (__syncthreads_or(*abort_flag != 0u)) {
@@ -425,6 +433,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     if (stop) break;
   }
+  if (tid == 0) bulk_wait_group0();   // dQ reductions complete
   // a Q / dO load issued ahead lands before the CTA can exit (only after an abort)
   if (tid == 0 && q_in_flight) {
     const uint64_t t0 = globaltimer_ns();

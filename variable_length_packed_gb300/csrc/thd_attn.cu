@@ -82,6 +82,21 @@ bool encode_thd_map(CUtensorMap* map, const void* base, int rows, int heads, int
   return r == CUDA_SUCCESS;
 }
 
+// 2-D view [rows, cols] of an fp32 array, box = 128 rows x 32 columns (128 bytes),
+// 128-byte swizzle: the target of the backward pass's dQ tile reductions.
+bool encode_f32_map(CUtensorMap* map, const void* base, int rows, long long cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4ull};
+  cuuint32_t box[2] = {32u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <typename DT, int DP, bool kTMA>
 int launch_serial(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const thd::AttnParams& p,
                   int grid, cudaStream_t stream) {
@@ -120,7 +135,7 @@ size_t bwd_workspace_bytes(int T, int Hq, int d) {
 
 template <typename DT, int DP>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-               const thd::BwdParams& bp, int sms, cudaStream_t stream) {
+               const CUtensorMap& mdq, const thd::BwdParams& bp, int sms, cudaStream_t stream) {
   const int small_grid = sms * 8;
   thd::attn_bwd_pre_kernel<DT><<<small_grid, 256, 0, stream>>>(bp);
   if (cudaGetLastError() != cudaSuccess) return THD_ERR_CUDA;
@@ -128,7 +143,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const size_t smem = one_cta_per_sm(sizeof(thd::BwdSmem<DP>) + 1024);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return THD_ERR_CUDA;
-  kern<<<sms, thd::kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, bp);
+  kern<<<sms, thd::kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, bp);
   if (cudaGetLastError() != cudaSuccess) return THD_ERR_CUDA;
   thd::attn_bwd_post_kernel<DT><<<small_grid, 256, 0, stream>>>(bp);
   return cudaGetLastError() == cudaSuccess ? THD_OK : THD_ERR_CUDA;
@@ -214,18 +229,19 @@ int thd_attn_bwd_window(const void* q, const void* k, const void* v, const void*
 
   if (cudaMemsetAsync(workspace, 0, 16, st) != cudaSuccess) return THD_ERR_CUDA;
   const bool bf16 = dtype == THD_BF16;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!encode_thd_map(&mq, q, total_tokens, num_heads_q, head_dim, bf16) ||
       !encode_thd_map(&mk, k, total_tokens, num_heads_kv, head_dim, bf16) ||
       !encode_thd_map(&mv, v, total_tokens, num_heads_kv, head_dim, bf16) ||
-      !encode_thd_map(&mdo, dout, total_tokens, num_heads_q, head_dim, bf16))
+      !encode_thd_map(&mdo, dout, total_tokens, num_heads_q, head_dim, bf16) ||
+      !encode_f32_map(&mdq, bp.dacc, total_tokens, (long long)num_heads_q * head_dim))
     return THD_ERR_CUDA;
   if (bf16) {
-    if (head_dim == 128) return launch_bwd<__nv_bfloat16, 128>(mq, mk, mv, mdo, bp, sms, st);
-    return launch_bwd<__nv_bfloat16, 64>(mq, mk, mv, mdo, bp, sms, st);
+    if (head_dim == 128) return launch_bwd<__nv_bfloat16, 128>(mq, mk, mv, mdo, mdq, bp, sms, st);
+    return launch_bwd<__nv_bfloat16, 64>(mq, mk, mv, mdo, mdq, bp, sms, st);
   }
-  if (head_dim == 128) return launch_bwd<__half, 128>(mq, mk, mv, mdo, bp, sms, st);
-  return launch_bwd<__half, 64>(mq, mk, mv, mdo, bp, sms, st);
+  if (head_dim == 128) return launch_bwd<__half, 128>(mq, mk, mv, mdo, mdq, bp, sms, st);
+  return launch_bwd<__half, 64>(mq, mk, mv, mdo, mdq, bp, sms, st);
 }
 
 int thd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
