@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             sm.dd[tid] = 0.f;
           }
         }
+        if (tid == 0) bulk_wait_group_read0();   // the previous tile's dQ staging was read
         __syncthreads();
         // ---- S^T = K Q^T, dP^T = V dO^T ----
         if (tid == 0) {
@@ -351,13 +352,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ph_mma ^= 1u;
         tc_fence_after();
         first = false;
-        // Q and dO are free once these MMAs completed: the next query tile of the
-        // item loads while this tile's dQ goes out
-        if (tid == 0 && !*abort_flag) {
-          if (qt + 1 < nqt) load_q(h, s.q_start + (qt + 1) * kTileM);
-          else if (hh + 1 < p.group) load_q(h + 1, s.q_start + qt_first * kTileM);
-        }
-
         // ---- dQ tile into the fp32 accumulator: 64 columns at a time through the dS^T
         // buffer (free once the dQ MMA completed) and a bulk tensor reduction ----
 #pragma unroll
@@ -377,9 +371,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_reduce_add_2d(&tm_dq, sm.ds, h * p.d + 64 * r, s.q_start + q0);
             tma_reduce_add_2d(&tm_dq, sm.ds + 16384, h * p.d + 64 * r + 32, s.q_start + q0);
             bulk_commit_group();
-            bulk_wait_group_read0();   // the buffer is free again
+            // Q and dO are free since the MMAs completed: after the last reduction the
+            // next query tile of the item loads while this tile's dQ goes out
+            if (r == DP / 64 - 1 && !*abort_flag) {
+              if (qt + 1 < nqt) load_q(h, s.q_start + (qt + 1) * kTileM);
+              else if (hh + 1 < p.group) load_q(h + 1, s.q_start + qt_first * kTileM);
+            }
           }
-          __syncthreads();
+          if (r + 1 < DP / 64) {   // the buffer is needed again at once; after the last
+            if (tid == 0) bulk_wait_group_read0();   // round it is waited for before the
+            __syncthreads();                         // next tile writes dS^T into it
+          }
         }
         tc_fence_before();
         if (__syncthreads_or(*abort_flag != 0u)) {
