@@ -245,20 +245,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     bool first = true;
     bool stop = false;
+    // LSE * log2(e) and D of query row tid of a tile (zero past the sequence)
+    auto row_stats = [&](int h, int q0, float& l2, float& dd) {
+      l2 = 0.f;
+      dd = 0.f;
+      if (tid < min(kTileM, s.q_len - q0)) {
+        const size_t li = (size_t)h * p.T + s.q_start + q0 + tid;
+        l2 = p.lse[li] * 1.4426950408889634f;
+        dd = bp.D[li];
+      }
+    };
+    float nl2 = 0.f, ndd = 0.f;   // the next tile's row statistics, loaded during this tile
+    if (any && tid < kTileM) row_stats(g * p.group, qt_first * kTileM, nl2, ndd);
     for (int hh = 0; any && hh < p.group && !stop; ++hh) {
       const int h = g * p.group + hh;
       for (int qt = qt_first; qt < nqt; ++qt) {
         const int q0 = qt * kTileM;
         const int rows_q = min(kTileM, s.q_len - q0);
         if (tid < kTileM) {
-          if (tid < rows_q) {
-            const size_t li = (size_t)h * p.T + s.q_start + q0 + tid;
-            sm.lse2[tid] = p.lse[li] * 1.4426950408889634f;
-            sm.dd[tid] = bp.D[li];
-          } else {
-            sm.lse2[tid] = 0.f;
-            sm.dd[tid] = 0.f;
-          }
+          sm.lse2[tid] = nl2;
+          sm.dd[tid] = ndd;
         }
         if (tid == 0) bulk_wait_group_read0();   // the previous tile's dQ staging was read
         __syncthreads();
@@ -285,6 +291,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
         ph_mma ^= 1u;
         tc_fence_after();
+
+        if (tid < kTileM) {   // the next tile's statistics load while this one computes
+          if (qt + 1 < nqt) row_stats(h, q0 + kTileM, nl2, ndd);
+          else if (hh + 1 < p.group) row_stats(h + 1, qt_first * kTileM, nl2, ndd);
+        }
 
         // ---- P^T and dS^T for this thread's key row and column half ----
         // query column c of the tile sees this key iff c_lo <= c <= c_hi (query
