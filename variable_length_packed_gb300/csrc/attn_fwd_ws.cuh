@@ -6,7 +6,8 @@
 //
 //   warp 0      scheduler + TMA producer: claims items from the global counter,
 //               publishes them to the other warps, loads Q (both tiles) and the
-//               K/V tiles of the item into a two-stage ring.
+//               K/V tiles of the item into a ring (2 stages at head_dim 128, 4
+//               at 64).
 //   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM (SS UMMA),
 //               then O_i += P_i V_j with P_i read from TMEM (TS UMMA); the two
 //               tiles alternate so one tile's softmax overlaps the other
@@ -27,10 +28,14 @@
 //
 // Short sequences (at most 128 query rows and 128 keys) are not blocked by
 // 256 rows: their (sequence, head) tiles are paired, two independent tiles per
-// work unit, each with its own K/V tile, and the MMA warp issues the next
-// unit's S_t right after this unit's P_t V (S_0' after P_0 V, S_1' after P_1
-// V), so the two softmax warpgroups alternate across units the way they
-// alternate across KV tiles of a long sequence.
+// work unit, each with its own K/V tile, and the MMA warp issues each tile's
+// P_t V and then the next unit's S_t as soon as their inputs are ready (the
+// barriers of both tiles are polled), so the two softmax warpgroups alternate
+// across units the way they alternate across KV tiles of a long sequence.
+//
+// With a sliding window (kWin), a Q tile visits only the KV tiles inside its
+// rows' bands, starting at its own first tile, and rows mask keys on both
+// sides; the kernel without a window is a separate instantiation.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; P_i
 // occupies the first 64 columns of S_i (two 16-bit values per column).
