@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_2d(sm.k + pn * 16384, &tm_k, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
         tma_load_2d(sm.v + pn * 16384, &tm_v, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
       }
+      bulk_wait_group_read0();   // the previous item's last dQ staging (in dO) was read
       load_q(g * p.group, s.q_start + qt_first * kTileM);   // the item's first query tile
     }
     bool first = true;
@@ -363,35 +364,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ph_mma ^= 1u;
         tc_fence_after();
         first = false;
-        // ---- dQ tile into the fp32 accumulator: 64 columns at a time through the dS^T
-        // buffer (free once the dQ MMA completed) and a bulk tensor reduction ----
+        // ---- dQ tile into the fp32 accumulator by bulk tensor reductions, 64 columns
+        // at a time, staged in buffers free once the MMAs completed: the dS^T buffer,
+        // then (head_dim 128) the dO buffer ----
 #pragma unroll
         for (int r = 0; r < DP / 64; ++r) {
-          const int c = 2 * r + half;   // 32-column chunk: panel `half` of the buffer
+          const int c = 2 * r + half;   // 32-column chunk: panel `half` of the staging buffer
+          uint8_t* stage = r == 0 ? sm.ds : sm.dout;
           uint32_t o[32];
           tmem_ld32(tS + t_lane + 32 * c, o);
           tmem_ld_wait_regs32(o);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint4*>(sm.ds + sw128_offset(row, 8 * half + e)) =
+            *reinterpret_cast<uint4*>(stage + sw128_offset(row, 8 * half + e)) =
                 make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
           fence_proxy_async_smem();
           __syncthreads();
           if (tid == 0) {
             // rows past the sequence carry dS = 0, so their (zero) rows add nothing
-            tma_reduce_add_2d(&tm_dq, sm.ds, h * p.d + 64 * r, s.q_start + q0);
-            tma_reduce_add_2d(&tm_dq, sm.ds + 16384, h * p.d + 64 * r + 32, s.q_start + q0);
+            tma_reduce_add_2d(&tm_dq, stage, h * p.d + 64 * r, s.q_start + q0);
+            tma_reduce_add_2d(&tm_dq, stage + 16384, h * p.d + 64 * r + 32, s.q_start + q0);
             bulk_commit_group();
-            // Q and dO are free since the MMAs completed: after the last reduction the
-            // next query tile of the item loads while this tile's dQ goes out
-            if (r == DP / 64 - 1 && !*abort_flag) {
-              if (qt + 1 < nqt) load_q(h, s.q_start + (qt + 1) * kTileM);
-              else if (hh + 1 < p.group) load_q(h + 1, s.q_start + qt_first * kTileM);
-            }
           }
-          if (r + 1 < DP / 64) {   // the buffer is needed again at once; after the last
-            if (tid == 0) bulk_wait_group_read0();   // round it is waited for before the
-            __syncthreads();                         // next tile writes dS^T into it
+        }
+        // The next query tile of the item loads while this tile's dQ goes out; its dO
+        // lands in a staging buffer only once the reductions have read it.  (The dS^T
+        // buffer's read is waited for before the next tile writes dS^T.)
+        if (tid == 0 && !*abort_flag) {
+          const bool more = qt + 1 < nqt || hh + 1 < p.group;
+          if (more) {
+            const int nh = qt + 1 < nqt ? h : h + 1;
+            const int nrow = s.q_start + (qt + 1 < nqt ? (qt + 1) * kTileM : qt_first * kTileM);
+            if (DP > 64) bulk_wait_group_read0();
+            load_q(nh, nrow);
           }
         }
         tc_fence_before();

@@ -214,7 +214,7 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   constexpr int kPanels = DP / 64;
   constexpr int kQSlots = WsSmem<DP>::kQSlots, kWsStages = WsSmem<DP>::kStages;
   const int lane = threadIdx.x & 31;
-  uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, k_issued = 0, v_issued = 0;
+  uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0;
   bool ok = true;
   Claimer claimer{0ull, 0};
   for (;;) {
@@ -256,14 +256,12 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
         if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.k_empty[st], reuse);
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-        ++k_issued;
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
           tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], kvh * p.d + pn * 64, row);
         if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.v_empty[st], reuse);
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-        ++v_issued;
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
           tma_load_2d(sm.v[st] + pn * 16384, tm_v, &sm.v_full[st], kvh * p.d + pn * 64, row);
@@ -277,12 +275,10 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   if (lane == 0) {
     for (uint32_t c = (q_cnt > (uint32_t)kQSlots ? q_cnt - kQSlots : 0); c < q_cnt; ++c)
       drain_wait(&sm.q_full[c % kQSlots], (c / kQSlots) & 1);
-    // (K and V loads are counted separately: a wait that gave up may leave a
-    // stage's V load unissued after its K load)
-    for (uint32_t c = (k_issued > (uint32_t)kWsStages ? k_issued - kWsStages : 0); c < k_issued; ++c)
+    for (uint32_t c = (kv_cnt > (uint32_t)kWsStages ? kv_cnt - kWsStages : 0); c < kv_cnt; ++c) {
       drain_wait(&sm.k_full[c % kWsStages], (c / kWsStages) & 1);
-    for (uint32_t c = (v_issued > (uint32_t)kWsStages ? v_issued - kWsStages : 0); c < v_issued; ++c)
       drain_wait(&sm.v_full[c % kWsStages], (c / kWsStages) & 1);
+    }
   }
   __syncwarp();
 }
@@ -780,6 +776,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (sm.abort != 0u && threadIdx.x == 0) {
+    // after a wait gave up, a K copy issued just before may still be in flight
+    // (the producer drains the stages it completed): let it land
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) {
+    }
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
