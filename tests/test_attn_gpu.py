@@ -257,3 +257,15 @@ def test_non_monotone_metadata_does_not_fault():
                      0.125, workspace=ws)
     torch.cuda.synchronize()
     assert status_word(ws) == 0
+
+
+def test_results_do_not_depend_on_the_max_seqlen_hint():
+    """max_seqlen only sizes the scheduler's claim batches: any value gives the same bits."""
+    lens = [700, 1, 129, 90, 300, 0, 257, 41, 128, 513] * 3
+    w = workloads.from_lengths("hint", lens, [i % 3 == 0 for i in range(len(lens))], heads_q=4, heads_kv=2,
+                               head_dim=64, dtype=torch.bfloat16, seed=21)
+    dev = to_device(w)
+    outs = [run_gpu(w, dev=dev, max_seqlen=hint) for hint in (w.max_seqlen, 1, 16, 1 << 20)]
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    compare_full(w, *outs[0])
