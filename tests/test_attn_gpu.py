@@ -269,3 +269,23 @@ def test_results_do_not_depend_on_the_max_seqlen_hint():
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
     compare_full(w, *outs[0])
+
+
+def test_binding_rejects_short_metadata_and_wrong_outputs():
+    """The kernels read batch_size + 1 cu_seqlens entries: a shorter buffer, or an output of
+    the wrong shape, is refused before anything is launched."""
+    w = workloads.make("tiny_mixed")
+    dev = to_device(w)
+    B = w.batch_size
+    with pytest.raises(ValueError):
+        vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], batch_size=B + 1)
+    with pytest.raises(ValueError):
+        vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], seq_is_causal=dev["causal"][:B - 1],
+                         batch_size=B)
+    with pytest.raises(ValueError):
+        vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], batch_size=B,
+                         out=torch.empty_like(dev["q"])[:-1])
+    with pytest.raises(ValueError):
+        vlp.thd_padding_mask(dev["cu"], B + 1, 8)
+    with pytest.raises(ValueError):
+        vlp.thd_padding_mask(dev["cu"], B, 8, mask=torch.empty(B * 8 - 1, dtype=torch.bool, device="cuda"))

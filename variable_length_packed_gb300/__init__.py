@@ -99,6 +99,25 @@ def _cuda(t, name):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_metadata(batch_size, cu_q, cu_kv=None, pad_q=None, pad_kv=None, flags=None):
+    """The kernels read entries 0..batch_size of cu_seqlens*, 0..batch_size-1 of the padded
+    starts and the per-sequence flags: the buffers must hold them (longer is fine)."""
+    if int(batch_size) < 0:
+        raise ValueError("batch_size must be >= 0")
+    if int(batch_size) == 0:
+        return
+    for name, t, need in (("cu_seqlens_q", cu_q, batch_size + 1), ("cu_seqlens_kv", cu_kv, batch_size + 1),
+                          ("cu_seqlens_q_padded", pad_q, batch_size), ("cu_seqlens_kv_padded", pad_kv, batch_size),
+                          ("seq_is_causal", flags, batch_size)):
+        if t is not None and t.numel() < need:
+            raise ValueError(f"{name} holds {t.numel()} entries, batch_size {batch_size} needs {need}")
+
+
+def _check_out(t, name, shape, dtype, device):
+    if t is not None and (tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device):
+        raise ValueError(f"{name} must be a {dtype} tensor of shape {tuple(shape)} on {device}")
+
+
 def _stream_handle(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -145,6 +164,10 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
         raise TypeError("seq_is_causal must be bool or uint8")
     if batch_size is None:
         batch_size = cu_seqlens_q.numel() - 1
+    _check_metadata(batch_size, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                    seq_is_causal)
+    _check_out(out, "out", q.shape, q.dtype, q.device)
+    _check_out(lse, "lse", (Hq, T), torch.float32, q.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -182,6 +205,10 @@ def thd_attn_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padd
     if out is None:
         raise ValueError("out must be provided")
     T, Hq, d = q.shape
+    _check_metadata(batch_size, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                    seq_is_causal)
+    _check_out(out, "out", q.shape, q.dtype, q.device)
+    _check_out(lse, "lse", (Hq, T), torch.float32, q.device)
     with torch.cuda.device(q.device):
         st = _lib().thd_attn_fwd_noalloc(
             _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
@@ -200,6 +227,9 @@ def thd_padding_mask(cu_seqlens, batch_size, max_seqlen, mask=None):
     _cuda(mask, "mask")
     if cu_seqlens.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
+    _check_metadata(batch_size, cu_seqlens)
+    if mask is not None and (mask.numel() != int(batch_size) * int(max_seqlen) or mask.element_size() != 1):
+        raise ValueError("mask must hold batch_size * max_seqlen one-byte elements")
     if mask is None:
         mask = torch.empty((batch_size, 1, 1, max_seqlen), dtype=torch.bool, device=cu_seqlens.device)
     with torch.cuda.device(cu_seqlens.device):
@@ -223,6 +253,8 @@ def thd_attn_merge(out_a, lse_a, out_b, lse_b, out=None, lse=None):
     if lse_a.shape != (H, T) or lse_b.shape != (H, T) or lse_a.dtype != torch.float32 \
             or lse_b.dtype != torch.float32:
         raise ValueError("lse_a and lse_b must be float32 [H, T]")
+    _check_out(out, "out", out_a.shape, out_a.dtype, out_a.device)
+    _check_out(lse, "lse", (H, T), torch.float32, out_a.device)
     if out is None:
         out = torch.empty_like(out_a)
     if lse is None:
@@ -246,6 +278,10 @@ def thd_padding_mask_cross(cu_seqlens_q, cu_seqlens_kv, batch_size, max_seqlen_q
     if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_kv.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
     dev = cu_seqlens_q.device
+    _check_metadata(batch_size, cu_seqlens_q, cu_seqlens_kv)
+    for name, m, sl in (("mask_q", mask_q, max_seqlen_q), ("mask_kv", mask_kv, max_seqlen_kv)):
+        if m is not None and (m.numel() != int(batch_size) * int(sl) or m.element_size() != 1):
+            raise ValueError(f"{name} must hold batch_size * max_seqlen one-byte elements")
     if mask_q is None:
         mask_q = torch.empty((batch_size, 1, 1, max_seqlen_q), dtype=torch.bool, device=dev)
     if mask_kv is None:
@@ -276,6 +312,11 @@ def thd_attn_bwd(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlen
         raise ValueError("out / dout must match q; lse must be float32 [Hq, T]")
     if batch_size is None:
         batch_size = cu_seqlens_q.numel() - 1
+    _check_metadata(batch_size, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                    seq_is_causal)
+    _check_out(dq, "dq", q.shape, q.dtype, q.device)
+    _check_out(dk, "dk", k.shape, k.dtype, k.device)
+    _check_out(dv, "dv", v.shape, v.dtype, v.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
