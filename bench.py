@@ -509,6 +509,16 @@ def run_gpu(args, ws, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, ws, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcu, hcausal))
     d2h = sum(t.numel() * t.element_size() for t in (hout, hlse, hmask))
+    # the box's pinned-copy bandwidths, one copy each way (untimed; explains e2e against value)
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    c0.record(stream)
+    q.copy_(hq, non_blocking=True)
+    c1.record(stream)
+    hout.copy_(out, non_blocking=True)
+    c2.record(stream)
+    torch.cuda.synchronize()
+    copy_gbs = {"h2d_gbs": hq.numel() * hq.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9,
+                "d2h_gbs": hout.numel() * hout.element_size() / (c1.elapsed_time(c2) * 1e-3) / 1e9}
     del sets[1]
 
     # ---- check the timed output once against the oracle on a few rows (not timed) ----
@@ -536,7 +546,7 @@ def run_gpu(args, ws, rank, local):
                  "frac": mask_gbs / peaks["hbm_gbs"], "algorithmic_bytes": mask_bytes,
                  "timing": f"CUDA graph of {reps} back-to-back launches", "traffic": recorded_traffic("padding_mask")},
         "e2e": {"value": ws * eff / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "copy_bandwidth": copy_gbs,
                 "pipelining": "two buffer sets; step i+1's H2D and step i-1's D2H overlap step i's kernels"},
         "other_workloads": others,
         "backward": backward,
