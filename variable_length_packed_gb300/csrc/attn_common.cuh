@@ -264,7 +264,13 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
     uint32_t it = 0u;
     if (j < n) {
       const SeqInfo sj = cached_seq(s, s.order[j], p);
-      it = (kPairs && seq_is_short(sj)) ? 0u : seq_items<BLOCK_M, kKvSide>(sj, p);
+      if (kPairs && seq_is_short(sj)) {
+        it = 0u;
+      } else if (kPairs && (p.group & 1) == 0) {   // grouped heads: 128-row blocks of two heads
+        it = (uint32_t)((sj.q_len + kTileM - 1) / kTileM) * (uint32_t)(p.Hq / 2);
+      } else {
+        it = seq_items<BLOCK_M, kKvSide>(sj, p);
+      }
     }
     const uint32_t incl = warp_incl_scan(it);
     if (j < n) s.cum[j + 1] = carry + incl;

@@ -1,8 +1,10 @@
 // attn_fwd_ws.cuh — the persistent, warp-specialised attention kernel
 // (head_dim 64 or 128, TMA loads).
 //
-// One CTA per SM.  A work item is a block of 256 query rows of one (sequence,
-// head), split into two 128-row Q tiles that share every K/V tile:
+// One CTA per SM.  A work item is two 128-row Q tiles of one sequence that share
+// every K/V tile: the same 128 rows of two query heads of one group when the
+// number of query heads per K/V head is even, else a block of 256 rows of one
+// query head:
 //
 //   warp 0      scheduler + TMA producer: claims items from the global counter,
 //               publishes them to the other warps, loads Q (both tiles) and the
@@ -26,8 +28,8 @@
 // MMAs.  K and V stages are released separately: a K stage once both tiles'
 // S MMAs on it are done, a V stage once both P V MMAs are done.
 //
-// Short sequences (at most 128 query rows and 128 keys) are not blocked by
-// 256 rows: their (sequence, head) tiles are paired, two independent tiles per
+// Short sequences (at most 128 query rows and 128 keys) are not blocked that
+// way: their (sequence, head) tiles are paired, two independent tiles per
 // work unit, each with its own K/V tile, and the MMA warp issues each tile's
 // P_t V and then the next unit's S_t as soon as their inputs are ready (the
 // barriers of both tiles are polled), so the two softmax warpgroups alternate
@@ -60,8 +62,8 @@ struct WsTile {
   int j0, n;     // KV tiles the tile visits: [j0, n); n = 0 when no row sees a key
 };
 
-// Work unit: one block of 256 query rows of a long sequence (two tiles sharing
-// every K/V tile, `paired` = 0), or two independent short (sequence, head)
+// Work unit: two Q tiles of a long sequence (two heads of one group over the
+// same 128 rows, or 256 rows of one head; both share every K/V tile, `paired` = 0), or two independent short (sequence, head)
 // tiles, each with its own single K/V tile (`paired` = 1).
 struct WsUnit {
   int valid;
@@ -107,7 +109,7 @@ struct WsSmem {
 };
 
 // Maps global unit index w to its work unit (one full warp; w never decreases
-// within a CTA).  Units of a chunk: the long sequences' 256-row blocks in the
+// within a CTA).  Units of a chunk: the long sequences' two-tile blocks in the
 // scheduler's order, then the short sequences' (sequence, head) tiles, heads
 // innermost, two per unit.
 template <bool kWin>
@@ -125,14 +127,19 @@ __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, u
     const int pos = sched_find(s, local);
     const SeqInfo seq = cached_seq(s, s.order[pos], p);
     const uint32_t r = local - s.cum[pos];
-    const uint32_t nblk = (uint32_t)((seq.q_len + kWsBlockM - 1) / kWsBlockM);
-    const int h = (int)(r / nblk);
+    // Grouped query heads (an even number per key/value head): the two tiles are the
+    // same 128 rows of two heads of one group, so they visit the same KV tiles.
+    // Otherwise: two consecutive 128-row blocks of one head.
+    const bool head_pair = (p.group & 1) == 0;
+    const int rows_blk = head_pair ? kTileM : kWsBlockM;
+    const uint32_t nblk = (uint32_t)((seq.q_len + rows_blk - 1) / rows_blk);
+    const int hsel = (int)(r / nblk);
     const int qb = (int)(nblk - 1u - r % nblk);   // heaviest (last) block first
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       u.t[t].seq = seq;
-      u.t[t].h = h;
-      u.t[t].q0 = qb * kWsBlockM + t * kTileM;
+      u.t[t].h = head_pair ? 2 * hsel + t : hsel;
+      u.t[t].q0 = head_pair ? qb * kTileM : qb * kWsBlockM + t * kTileM;
       ws_tile_range<kWin>(u.t[t]);
     }
     // tile 0's rows come first, so its window starts no later than tile 1's
