@@ -84,7 +84,14 @@ size_t thd_attn_workspace_size(void);
  *              per-sequence policy review comment of the same PR.  Rows that
  *              see no key are written as 0 with lse -inf.
  * batch_size   >= 0.  0 writes zeros to every row of `out` (and -inf to lse).
- * max_seqlen   >= 0; a sizing hint only (the kernels read the true lengths).
+ * max_seqlen   >= 0; a hint only (the kernels read the true lengths, and any value
+ *              gives results within the parity bounds).  It sizes the scheduler's
+ *              claim batches and, for head_dim 64 / 128 without a window, picks the
+ *              tile layout of short sequences: with 1 <= max_seqlen <= 256, runs of
+ *              consecutive sequences of at most 128 rows and keys share a tile;
+ *              otherwise each (sequence, head) has its own.  Calls with hints on the
+ *              same side of 256 give the same bits; across it, short sequences'
+ *              rows may differ in the last place.
  * softmax_scale finite, > 0.
  * out          device, [T, Hq, head_dim], dtype.  Rows of no sequence (gaps,
  *              leading and trailing pad) are written as exact zeros.

@@ -3,7 +3,8 @@
 Small workloads are compared on every row; the large ones (mixed-policy GQA, long
 context, many short sequences) on sampled (sequence, head, row) triples computed one by
 one by the oracle, plus every pad row (exact zero / -inf LSE).  Tolerances: |out| 1e-2
-for bf16 inputs, 2e-3 for fp16, |LSE| 1e-3.
+for bf16 inputs, 2e-3 for fp16 (an element above them passes only within that plus half an
+output-type ulp of the exact value, at most one in 10^4: see thd_testutil.out_bound), |LSE| 1e-3.
 """
 import math
 
@@ -14,8 +15,8 @@ import torch
 import oracle
 import workloads
 from conftest import read_golden
-from thd_testutil import (LSE_ATOL, OUT_ATOL, boundary_rows, check_pad_rows, compare_full, compare_sampled,
-                          run_gpu, to_device, valid_rows)
+from thd_testutil import (LSE_ATOL, assert_out_close, boundary_rows, check_pad_rows, compare_full,
+                          compare_sampled, run_gpu, to_device, valid_rows)
 
 pytestmark = pytest.mark.gpu
 vlp = pytest.importorskip("variable_length_packed_gb300")
@@ -67,9 +68,10 @@ def test_two_call_identity_on_gpu():
                                     ints("full_call.cu_seqlens_padded"), None, 3, 4, w.softmax_scale)
     out, lse = run_gpu(w, dev=dev)
     torch.cuda.synchronize()
-    # each row is computed by the same tile arithmetic in both forms: equal bit for bit
-    assert torch.equal(out_c + out_f, out)
-    assert torch.equal(torch.logaddexp(lse_c, lse_f), lse)
+    # The three calls pack their sequences into tiles differently (a sequence's keys sit
+    # at other tile columns, so sums round in another order): the sum of the two calls and
+    # the mixed call are each held to the oracle's tolerances.
+    compare_full(w, out_c + out_f, torch.logaddexp(lse_c, lse_f))
     compare_full(w, out, lse)
 
 
@@ -122,11 +124,14 @@ def test_head_dims_and_tile_boundaries(d, dtype):
     compare_full(w, out, lse)
 
 
+@pytest.mark.parametrize("hint", [0, 128])
 @pytest.mark.parametrize("d,dtype", [(64, torch.float16), (128, torch.bfloat16)])
-def test_paired_short_tiles_across_chunks(d, dtype):
-    """Sequences of at most 128 rows run as independent (sequence, head) tiles two per unit,
-    longer ones as 256-row blocks: 700 sequences (two scheduler chunks of 512), three query
-    heads on one KV head (odd tile counts per chunk), zero-length sequences, lengths 128 / 129."""
+def test_paired_short_tiles_across_chunks(d, dtype, hint):
+    """Sequences of at most 128 rows run as short tiles, two per unit ((sequence, head) tiles
+    with the hint 0, runs of consecutive short sequences packed into 128-row tiles with the
+    hint 128), longer ones as 256-row blocks: 700 sequences (two scheduler chunks of 512),
+    three query heads on one KV head (odd tile counts per chunk), zero-length sequences (they
+    end a run), lengths 128 / 129."""
     rng = np.random.default_rng(70 + d)
     B = 700
     lens = rng.integers(1, 129, size=B)
@@ -138,7 +143,7 @@ def test_paired_short_tiles_across_chunks(d, dtype):
     w = workloads.from_lengths("paired", lens, causal, gaps_before=gaps, trailing=5, heads_q=3, heads_kv=1,
                                head_dim=d, dtype=dtype, seed=d, with_padded=True)
     ws = workspace()
-    out, lse = run_gpu(w, workspace=ws)
+    out, lse = run_gpu(w, workspace=ws, max_seqlen=hint)
     assert status_word(ws) == 0
     compare_full(w, out, lse)
 
@@ -171,11 +176,69 @@ def test_paired_short_cross_sequences(d, dtype):
     o = out.float().cpu().double().numpy()
     l = lse.cpu().double().numpy()
     seen = np.isfinite(ref_lse)
-    assert np.abs(o - ref).max() <= OUT_ATOL[dtype]
+    assert_out_close(o, ref, dtype, "cross")
     assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
     assert np.all(np.isneginf(l[~seen]))
     assert np.all(o[~seen.any(axis=0)] == 0.0)
     assert (~seen).sum() > 0
+
+
+@pytest.mark.parametrize("d,dtype", [(64, torch.float16), (128, torch.bfloat16)])
+def test_packed_tiles_of_tiny_sequences(d, dtype):
+    """Runs of tiny sequences without gaps fill a packed tile with up to 128 sequences of one
+    row; runs that end exactly at a tile's last row or key; all three mask types; members
+    whose key span is empty or longer / shorter than their query span."""
+    rng = np.random.default_rng(110 + d)
+    B = 600
+    lq = rng.integers(1, 4, size=B)
+    lq[:128] = 1                                   # one group of 128 one-row sequences
+    lq[128:130] = [64, 64]                         # a group that ends at row 127
+    lkv = lq.copy()
+    sel = rng.choice(np.arange(130, B), 80, replace=False)
+    lkv[sel] = rng.integers(0, 6, size=80)
+    codes = rng.integers(0, 3, size=B).astype(np.uint8)
+    q_gap = np.where(rng.random(B) < 0.2, rng.integers(1, 5, size=B), 0)
+    q_gap[:130] = 0
+    q_starts = np.concatenate([[0], np.cumsum(lq + q_gap)[:-1]]).astype(np.int32)
+    kv_starts = (np.concatenate([[0], np.cumsum(lkv)[:-1]]) + 3).astype(np.int32)
+    T = int(max(q_starts[-1] + lq[-1], kv_starts[-1] + lkv[-1]) + 4)
+    w = workloads.from_lengths("tiny", [T], [0], heads_q=4, heads_kv=2, head_dim=d, dtype=dtype, seed=d + 3)
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    ws = workspace()
+    out, lse = vlp.thd_attn_fwd(w.q.cuda(), w.k.cuda(), w.v.cuda(), dev(cu_q), dev(cu_k), dev(q_starts),
+                                dev(kv_starts), dev(codes), B, 8, w.softmax_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert status_word(ws) == 0
+    ref, ref_lse = oracle.thd_attention_fwd_general(w.q, w.k, w.v, cu_q, cu_k, q_starts, kv_starts, codes, B,
+                                                    w.softmax_scale)
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    seen = np.isfinite(ref_lse)
+    assert_out_close(o, ref, dtype, "tiny")
+    assert np.array_equal(np.isfinite(l), seen)
+    assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
+
+
+def test_packing_is_decided_per_chunk():
+    """One launch, two scheduler chunks: in the first, every short sequence is followed by a
+    long one (nothing to pack: one tile per (sequence, head)); in the second, runs of tiny
+    sequences are packed.  Both kinds of short tile and the long blocks in one launch."""
+    rng = np.random.default_rng(123)
+    B = 700
+    lens = np.empty(B, dtype=np.int64)
+    lens[:512:2] = rng.integers(1, 129, size=256)
+    lens[1:512:2] = rng.integers(129, 300, size=256)
+    lens[512:] = rng.integers(1, 12, size=B - 512)
+    causal = rng.random(B) < 0.5
+    gaps = rng.integers(0, 4, size=B)
+    w = workloads.from_lengths("chunks", lens, causal, gaps_before=gaps, trailing=3, heads_q=2, heads_kv=1,
+                               head_dim=64, dtype=torch.bfloat16, seed=31, with_padded=True)
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws, max_seqlen=256)   # the packing layout
+    assert status_word(ws) == 0
+    compare_full(w, out, lse)
 
 
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
@@ -259,16 +322,26 @@ def test_non_monotone_metadata_does_not_fault():
     assert status_word(ws) == 0
 
 
-def test_results_do_not_depend_on_the_max_seqlen_hint():
-    """max_seqlen only sizes the scheduler's claim batches: any value gives the same bits."""
-    lens = [700, 1, 129, 90, 300, 0, 257, 41, 128, 513] * 3
+def test_max_seqlen_hint_picks_the_layout_not_the_result():
+    """max_seqlen sizes the claim batches and, up to 256, selects packed tiles for short
+    sequences: hints on the same side of 256 give the same bits, every hint is within the
+    oracle's bounds, and only rows of short sequences can differ across the two sides."""
+    lens = [700, 1, 129, 90, 300, 0, 257, 41, 128, 513, 7, 60, 3] * 3
     w = workloads.from_lengths("hint", lens, [i % 3 == 0 for i in range(len(lens))], heads_q=4, heads_kv=2,
                                head_dim=64, dtype=torch.bfloat16, seed=21)
     dev = to_device(w)
-    outs = [run_gpu(w, dev=dev, max_seqlen=hint) for hint in (w.max_seqlen, 1, 16, 1 << 20)]
-    for o, l in outs[1:]:
-        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
-    compare_full(w, *outs[0])
+    plain = [run_gpu(w, dev=dev, max_seqlen=hint) for hint in (w.max_seqlen, 0, 257, 1 << 20)]
+    packed = [run_gpu(w, dev=dev, max_seqlen=hint) for hint in (1, 16, 256)]
+    for group in (plain, packed):
+        for o, l in group[1:]:
+            assert torch.equal(o, group[0][0]) and torch.equal(l, group[0][1])
+        compare_full(w, *group[0])
+    rows = torch.zeros(w.total_tokens, dtype=torch.bool)
+    for st, L in zip(w.starts, w.lengths):
+        if L > 128:
+            rows[int(st):int(st) + int(L)] = True
+    rows = rows.cuda()
+    assert torch.equal(plain[0][0][rows], packed[0][0][rows])
 
 
 def test_binding_rejects_short_metadata_and_wrong_outputs():

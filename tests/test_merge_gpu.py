@@ -11,7 +11,7 @@ import oracle
 import workloads
 from conftest import read_golden
 from test_oracle_general import enumerate_cross_cases
-from thd_testutil import LSE_ATOL, OUT_ATOL
+from thd_testutil import LSE_ATOL, assert_out_close
 
 pytestmark = pytest.mark.gpu
 vlp = pytest.importorskip("variable_length_packed_gb300")
@@ -44,7 +44,7 @@ def test_mask_types_with_separate_q_kv(d, dtype):
     o = out.float().cpu().double().numpy()
     l = lse.cpu().double().numpy()
     seen = np.isfinite(ref_lse)
-    assert np.abs(o - ref).max() <= OUT_ATOL[dtype]
+    assert_out_close(o, ref, dtype, "merge")
     assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
     assert np.all(np.isneginf(l[~seen]))
     rows_none = ~seen.any(axis=0)
@@ -61,7 +61,7 @@ def test_merge_matches_oracle_on_synthetic_partials():
         o = out.float().cpu().double().numpy()
         l = lse.cpu().double().numpy()
         fin = np.isfinite(ref_lse)
-        assert np.abs(o - ref).max() <= OUT_ATOL[dtype], d
+        assert_out_close(o, ref, dtype, f"merge d={d}")
         assert np.abs(l[fin] - ref_lse[fin]).max() <= 1e-5
         assert np.all(np.isneginf(l[~fin])) and np.all(o[~fin.T] == 0)
 

@@ -13,7 +13,7 @@ import torch
 import oracle
 import workloads
 from test_bwd_gpu import REL
-from thd_testutil import LSE_ATOL, OUT_ATOL, to_device
+from thd_testutil import LSE_ATOL, assert_out_close, to_device
 
 pytestmark = pytest.mark.gpu
 vlp = pytest.importorskip("variable_length_packed_gb300")
@@ -52,7 +52,7 @@ def test_window_forward_matches_oracle(d, dtype):
         o = out.float().cpu().double().numpy()
         l = lse.cpu().double().numpy()
         seen = np.isfinite(ref_lse)
-        assert np.abs(o - ref).max() <= OUT_ATOL[dtype], window
+        assert_out_close(o, ref, dtype, f"window {window}")
         assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL, window
         assert np.all(np.isneginf(l[~seen])), window
         assert np.all(o[~seen.any(axis=0)] == 0.0), window
@@ -88,7 +88,7 @@ def test_window_with_separate_q_kv_sequences(window):
     o = out.float().cpu().double().numpy()
     l = lse.cpu().double().numpy()
     seen = np.isfinite(ref_lse)
-    assert np.abs(o - ref).max() <= OUT_ATOL[torch.bfloat16]
+    assert_out_close(o, ref, torch.bfloat16, "window cross")
     assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
     assert np.all(np.isneginf(l[~seen])) and np.all(o[~seen.any(axis=0)] == 0.0)
 

@@ -14,6 +14,34 @@ OUT_ATOL = {torch.bfloat16: 1e-2, torch.float16: 2e-3}
 LSE_ATOL = 1e-3
 
 
+def out_bound(ref, dtype):
+    """Per-element bound on |out - ref|: OUT_ATOL plus half a unit in the last place of the
+    output type at |ref|.  The output is stored in the input type, and from |ref| = 4 on a bf16
+    value correctly rounded from the exact one can itself be up to 0.0156 away from it, so the
+    flat 1e-2 cannot hold there; an element above OUT_ATOL passes only within this bound."""
+    mant = 7 if dtype == torch.bfloat16 else 10
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return OUT_ATOL[dtype] + np.where(a > 0, np.exp2(e - mant - 1), 0.0)
+
+
+def assert_out_close(got, ref, dtype, what=""):
+    """|got - ref| within out_bound everywhere, and above the flat OUT_ATOL in at most one
+    element in 10^4 (so the half-ulp allowance cannot hide a systematic error).  Returns the
+    largest error."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    if err.size == 0:
+        return 0.0
+    worst = float(err.max())
+    bound = out_bound(ref, dtype)
+    assert np.all(err <= bound), f"{what}: max |out err| {worst:.3e}, above the rounding bound"
+    over = int((err > OUT_ATOL[dtype]).sum())
+    assert over <= max(1, err.size // 10000), f"{what}: {over} of {err.size} elements above {OUT_ATOL[dtype]}"
+    return worst
+
+
 def to_device(w, device="cuda"):
     dev = torch.device(device)
     d = dict(
@@ -60,15 +88,13 @@ def compare_full(w, out, lse, ref_out=None, ref_lse=None):
             w.seq_is_causal, w.batch_size, w.softmax_scale)
     o = out.float().cpu().double().numpy()
     vr = valid_rows(w)
-    err = np.abs(o[vr] - ref_out[vr])
-    tol = OUT_ATOL[w.dtype]
-    assert err.max(initial=0.0) <= tol, f"{w.name}: max |out err| {err.max():.3e} > {tol}"
+    worst = assert_out_close(o[vr], ref_out[vr], w.dtype, w.name)
     if lse is not None:
         l = lse.cpu().double().numpy()
         lerr = np.abs(l[:, vr] - ref_lse[:, vr])
         assert lerr.max(initial=0.0) <= LSE_ATOL, f"{w.name}: max |lse err| {lerr.max():.3e}"
     check_pad_rows(w, out, lse)
-    return float(err.max(initial=0.0))
+    return worst
 
 
 def compare_sampled(w, out, lse, pairs, rows_for):
@@ -81,8 +107,7 @@ def compare_sampled(w, out, lse, pairs, rows_for):
         ref_o, ref_l = oracle.thd_attention_rows(w.q, w.k, w.v, s, s, L, bool(w.causal[b]), h, group,
                                                  w.softmax_scale, rows)
         got = out[s + torch.from_numpy(rows).to(out.device), h, :].float().cpu().double().numpy()
-        err = np.abs(got - ref_o).max()
-        assert err <= OUT_ATOL[w.dtype], f"{w.name} b={b} h={h}: |out err| {err:.3e}"
+        err = assert_out_close(got, ref_o, w.dtype, f"{w.name} b={b} h={h}")
         if lse is not None:
             gl = lse[h, s + torch.from_numpy(rows).to(lse.device)].cpu().double().numpy()
             lerr = np.abs(gl - ref_l).max()

@@ -139,20 +139,39 @@ __device__ __forceinline__ int kv_first_tile(const SeqInfo& s, int q0) { return 
 constexpr int kSchedChunk = 512;
 constexpr int kSchedBuckets = 1024;
 
+// Packed groups (kPack): runs of consecutive short sequences that fit one
+// 128-row Q window and one 128-key K/V window (built after the sort, in the
+// sort's histogram space).
+struct PackGroups {
+  uint16_t start[kSchedChunk];      // first chunk-local sequence of group g (batch order)
+  uint16_t end[kSchedChunk];        // one past its last
+  uint16_t next[kSchedChunk];       // per sequence: the first one that cannot join a group it starts
+  uint16_t jump[kSchedChunk];       // next applied 2^k times (reachability doubling)
+};
+
 struct SchedSmem {
-  uint32_t off[kSchedBuckets];      // histogram, then running bucket offsets
+  union {
+    uint32_t off[kSchedBuckets];    // histogram, then running bucket offsets (sort only)
+    PackGroups grp;                 // kPack, after the sort
+  };
   uint32_t cum[kSchedChunk + 1];    // exclusive prefix of item counts, sorted order
   int4 span[kSchedChunk];           // decoded (q_start, q_len, kv_start, kv_len) per chunk-local sequence
   uint8_t code[kSchedChunk];        // mask type code per chunk-local sequence
-  uint16_t key[kSchedChunk];        // sort key per chunk-local sequence
+  union {
+    uint16_t key[kSchedChunk];      // sort key per chunk-local sequence (sort only)
+    uint16_t reach[kSchedChunk];    // kPack: sequence starts a step of the greedy grouping
+  };
   uint16_t order[kSchedChunk];      // chunk-local sequence ids, sorted
   int chunk_base;
   int chunk_n;
   int n_short;                      // kPairs: short sequences, at sorted positions [n_long, n_long + n_short)
   int n_long;                       // kPairs: long sequences, at sorted positions [0, n_long)
+  int n_groups;                     // kPack: packed groups of short sequences
+  int pack_on;                      // kPack: this chunk's short sequences run as packed groups
   unsigned long long item_base;
   unsigned long long item_end;
 };
+static_assert(sizeof(PackGroups) <= sizeof(uint32_t) * kSchedBuckets, "groups fit the histogram space");
 
 // A short sequence fits one Q tile and one KV tile.  With kPairs (the
 // warp-specialised forward), short sequences are not split into BLOCK_M items:
@@ -160,6 +179,8 @@ struct SchedSmem {
 __device__ __forceinline__ bool seq_is_short(const SeqInfo& s) {
   return s.q_len > 0 && s.q_len <= kTileM && s.kv_len <= kBlockN;
 }
+// The same test on a chunk's cached (q_start, q_len, kv_start, kv_len).
+__device__ __forceinline__ bool span_is_short(int4 a) { return a.y > 0 && a.y <= kTileM && a.w <= kBlockN; }
 
 // Sort key (descending order = processing order).  Plain: KV tiles, full
 // context before causal at equal length.  kPairs: long sequences (keys >= 3)
@@ -211,9 +232,95 @@ __device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i, const A
   return si;
 }
 
+// Packs the chunk's short sequences (kPack): scanning in batch order, a group
+// starts at a short sequence and takes the following short sequences while their
+// rows and keys stay in order and inside 128 rows of the group's first row and
+// 128 keys of its first key; the next short sequence starts the next group.
+// The greedy scan is a chain start -> next(start) -> ...; it is walked with
+// pointer doubling (a sequence is on the chain iff it is reached from sequence 0
+// in fewer than n steps), so the warp needs log2(n) rounds instead of one step
+// per group.  When fewer than a quarter of the short sequences could take the
+// next one into their group, packing would save few tiles: the chunk keeps one
+// (sequence, head) tile per short sequence (pack_on = 0) and skips the doubling.
+// One full warp; s.off / s.key are free (the sort is done).
+__device__ void sched_pack_groups(SchedSmem& s, int n) {
+  const int lane = threadIdx.x & 31;
+  PackGroups& g = s.grp;
+  uint32_t joins = 0;   // short sequences whose group could take the next one
+  for (int i = lane; i < n; i += 32) {
+    const int4 a = s.span[i];
+    int nx = i + 1;
+    if (span_is_short(a)) {
+      int qe = a.x + a.y, ke = a.z + a.w;
+      while (nx < n) {
+        const int4 b = s.span[nx];
+        if (!span_is_short(b) || b.x < qe || b.z < ke || b.x + b.y > a.x + kTileM || b.z + b.w > a.z + kBlockN)
+          break;
+        qe = b.x + b.y;
+        ke = b.z + b.w;
+        ++nx;
+      }
+    }
+    g.next[i] = (uint16_t)nx;
+    g.jump[i] = (uint16_t)nx;
+    s.reach[i] = (uint16_t)(i == 0 ? 1 : 0);
+    joins += nx > i + 1 ? 1 : 0;
+  }
+  joins = __reduce_add_sync(0xffffffffu, joins);
+  if (4u * joins < (uint32_t)s.n_short) {
+    if (lane == 0) {
+      s.pack_on = 0;
+      s.n_groups = 0;
+    }
+    __syncwarp();
+    return;
+  }
+  __syncwarp();
+  const int rounds = n > 1 ? 32 - __clz(n - 1) : 0;   // 2^rounds >= n
+  for (int k = 0; k < rounds; ++k) {
+    // reached after m < 2^(k+1) steps: reached after m < 2^k, or 2^k steps past one
+    // (a lane may see another lane's new mark in the same round; it is on the chain too)
+    for (int i = lane; i < n; i += 32) {
+      const int j = g.jump[i];
+      if (s.reach[i] && j < n) s.reach[j] = 1;
+    }
+    __syncwarp();
+    uint16_t nj[kSchedChunk / 32];
+#pragma unroll
+    for (int t = 0; t < kSchedChunk / 32; ++t) {
+      const int i = lane + 32 * t;
+      const int j = i < n ? (int)g.jump[i] : n;
+      nj[t] = (uint16_t)(j < n ? (int)g.jump[j] : n);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < kSchedChunk / 32; ++t)
+      if (lane + 32 * t < n) g.jump[lane + 32 * t] = nj[t];
+    __syncwarp();
+  }
+  int ng = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    const bool st = i < n && s.reach[i] && span_is_short(s.span[i]);
+    const uint32_t m = __ballot_sync(0xffffffffu, st);
+    if (st) {
+      const int pos = ng + __popc(m & ((1u << lane) - 1u));
+      g.start[pos] = (uint16_t)i;
+      g.end[pos] = g.next[i];
+    }
+    ng += __popc(m);
+  }
+  if (lane == 0) {
+    s.n_groups = ng;
+    s.pack_on = 1;
+  }
+  __syncwarp();
+}
+
 // Load and sort the chunk of sequences starting at `base`.  One full warp.
-template <int BLOCK_M, bool kKvSide = false, bool kPairs = false>
+template <int BLOCK_M, bool kKvSide = false, bool kPairs = false, bool kPack = false>
 __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
+  static_assert(!kPack || kPairs, "packed groups replace the paired short tiles");
   const int lane = threadIdx.x & 31;
   const int n = min(kSchedChunk, p.B - base);
   for (int i = lane; i < kSchedBuckets; i += 32) s.off[i] = 0u;
@@ -282,6 +389,15 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
     s.chunk_n = n;
   }
   __syncwarp();
+  if (kPack) {   // a chunk without short sequences has no groups
+    if (s.n_short > 0) {
+      sched_pack_groups(s, n);
+    } else if (lane == 0) {
+      s.n_groups = 0;
+      s.pack_on = 0;
+    }
+    __syncwarp();
+  }
 }
 
 // Work item decoded from the global item index.
@@ -297,26 +413,28 @@ struct WorkItem {
 // heads, lowest block first (under causal masking the first keys are seen by
 // the most queries).
 // Items (units, with kPairs) of the loaded chunk: the long sequences' items,
-// then the short sequences' (sequence, head) tiles two per unit.
-template <bool kPairs>
+// then the short sequences' (sequence, head) tiles two per unit, or with kPack
+// the packed groups' (group, head) tiles two per unit.
+template <bool kPairs, bool kPack = false>
 __device__ __forceinline__ unsigned long long chunk_items(const SchedSmem& s, const AttnParams& p) {
   unsigned long long n = s.cum[s.chunk_n];
-  if (kPairs) n += ((unsigned long long)s.n_short * (unsigned long long)p.Hq + 1ull) / 2ull;
+  const int tiles = (kPack && s.pack_on) ? s.n_groups : s.n_short;
+  if (kPairs) n += ((unsigned long long)tiles * (unsigned long long)p.Hq + 1ull) / 2ull;
   return n;
 }
 
 // Loads later chunks until the one holding global item w; false when w is
 // past the last item.  One full warp.
-template <int BLOCK_M, bool kKvSide = false, bool kPairs = false>
+template <int BLOCK_M, bool kKvSide = false, bool kPairs = false, bool kPack = false>
 __device__ bool sched_seek(SchedSmem& s, const AttnParams& p, unsigned long long w) {
   while (w >= s.item_end) {
     const int next = s.chunk_base + s.chunk_n;
     if (next >= p.B) return false;
     const unsigned long long base_items = s.item_end;
-    sched_load_chunk<BLOCK_M, kKvSide, kPairs>(s, p, next);
+    sched_load_chunk<BLOCK_M, kKvSide, kPairs, kPack>(s, p, next);
     if ((threadIdx.x & 31) == 0) {
       s.item_base = base_items;
-      s.item_end = base_items + chunk_items<kPairs>(s, p);
+      s.item_end = base_items + chunk_items<kPairs, kPack>(s, p);
     }
     __syncwarp();
   }
@@ -375,6 +493,8 @@ __device__ __forceinline__ void sched_init(SchedSmem& s) {
   s.chunk_n = 0;
   s.n_short = 0;
   s.n_long = 0;
+  s.n_groups = 0;
+  s.pack_on = 0;
   s.item_base = 0;
   s.item_end = 0;
 }

@@ -29,7 +29,11 @@
 // S MMAs on it are done, a V stage once both P V MMAs are done.
 //
 // Short sequences (at most 128 query rows and 128 keys) are not blocked that
-// way: their (sequence, head) tiles are paired, two independent tiles per
+// way.  Without a window, runs of consecutive short sequences are packed into
+// one 128-row Q window and one 128-key K/V window each (a per-row table of
+// visible keys masks the other sequences' keys), in scheduler chunks where that
+// saves enough tiles; otherwise (and with a window) each (sequence, head) is its
+// own tile.  These tiles are paired, two independent tiles per
 // work unit, each with its own K/V tile, and the MMA warp issues each tile's
 // P_t V and then the next unit's S_t as soon as their inputs are ready (the
 // barriers of both tiles are polled), so the two softmax warpgroups alternate
@@ -63,15 +67,30 @@ struct WsTile {
 };
 
 // Work unit: two Q tiles of a long sequence (two heads of one group over the
-// same 128 rows, or 256 rows of one head; both share every K/V tile, `paired` = 0), or two independent short (sequence, head)
-// tiles, each with its own single K/V tile (`paired` = 1).
+// same 128 rows, or 256 rows of one head; both share every K/V tile, `paired` =
+// 0), or two independent tiles of short sequences, each with its own single K/V
+// tile (`paired` = 1).  A short tile is one (packed group, head) when the kernel
+// has no window and the chunk packs its short sequences (`packed` = 1: the
+// group's consecutive sequences share the tile's 128 rows and 128 keys, each row
+// seeing only its own sequence's keys), else one (sequence, head).
 struct WsUnit {
   int valid;
   int paired;
+  int packed;    // paired tiles of packed groups (row tables in the unit's slot)
   int jb;        // first KV tile loaded (shared: the smallest j0 of the tiles with work)
   int n_all;     // K/V tiles loaded for the unit: max(n) - jb shared, n0 + n1 paired
+  int g[2];      // packed tiles: chunk group of each tile (-1: no rows)
   WsTile t[2];
 };
+
+// Row table of a packed tile: per row, its first and last visible key as int16
+// tile columns (low / high half); rows of no sequence of the group are marked
+// kRowAbsent (no keys, no output).
+constexpr int kRowAbsent = 0x7FFF;
+__device__ __forceinline__ uint32_t row_keys(int first, int last) {
+  return ((uint32_t)first & 0xFFFFu) | ((uint32_t)last << 16);
+}
+constexpr uint32_t kRowAbsentKeys = ((uint32_t)kRowAbsent & 0xFFFFu) | (0xFFFFu << 16);   // (absent, -1)
 
 // What the MMA warp needs of a unit (the sequences' positions stay with the
 // producer and the softmax warps).
@@ -105,21 +124,27 @@ struct WsSmem {
   uint32_t tmem_base;
   uint32_t abort;
   WsUnit items[2];
+  uint32_t rows[2][2][kTileM];   // packed tiles' row tables, per item slot and tile
   SchedSmem sched;
 };
+// plus up to 1 KB to align the dynamic shared memory: within the 227 KB a CTA may use
+static_assert(sizeof(WsSmem<64>) + 1024 <= 227 * 1024 && sizeof(WsSmem<128>) + 1024 <= 227 * 1024,
+              "shared memory of the warp-specialised kernel");
 
 // Maps global unit index w to its work unit (one full warp; w never decreases
 // within a CTA).  Units of a chunk: the long sequences' two-tile blocks in the
-// scheduler's order, then the short sequences' (sequence, head) tiles, heads
-// innermost, two per unit.
-template <bool kWin>
+// scheduler's order, then the short tiles ((packed group, head) without a
+// window, (sequence, head) with one), heads innermost, two per unit.
+template <bool kWin, bool kPack>
 __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, unsigned long long w) {
   WsUnit u;
   u.valid = 0;
   u.paired = 0;
+  u.packed = 0;
   u.jb = 0;
   u.n_all = 0;
-  if (!sched_seek<kWsBlockM, false, true>(s, p, w)) return u;
+  u.g[0] = u.g[1] = -1;
+  if (!sched_seek<kWsBlockM, false, true, kPack>(s, p, w)) return u;
   u.valid = 1;
   const uint32_t local = (uint32_t)(w - s.item_base);
   const uint32_t n_long_items = s.cum[s.chunk_n];
@@ -148,13 +173,25 @@ __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, u
     u.n_all = jend > u.jb ? jend - u.jb : 0;
   } else {
     u.paired = 1;
-    const uint32_t total = (uint32_t)s.n_short * (uint32_t)p.Hq;
+    u.packed = (kPack && s.pack_on) ? 1 : 0;
+    const uint32_t total = (uint32_t)(u.packed ? s.n_groups : s.n_short) * (uint32_t)p.Hq;
     const uint32_t i0 = 2u * (local - n_long_items);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const uint32_t idx = i0 + t;
       WsTile& tt = u.t[t];
-      if (idx < total) {
+      if (idx < total && kPack && u.packed) {
+        // the group's rows [first q_start, last q end) and keys [first kv_start, last kv end)
+        const int g = (int)(idx / (uint32_t)p.Hq);
+        const int4 a = s.span[s.grp.start[g]];
+        const int4 e = s.span[s.grp.end[g] - 1];
+        u.g[t] = g;
+        tt.seq = SeqInfo{a.x, a.z, e.x + e.y - a.x, e.z + e.w - a.z, 0, 0, kNoBound, kNoBound};
+        tt.h = (int)(idx % (uint32_t)p.Hq);
+        tt.q0 = 0;
+        tt.j0 = 0;
+        tt.n = tt.seq.kv_len > 0 ? 1 : 0;
+      } else if (idx < total) {
         tt.seq = cached_seq(s, s.order[s.n_long + (int)(idx / (uint32_t)p.Hq)], p);
         tt.h = (int)(idx % (uint32_t)p.Hq);
         tt.q0 = 0;
@@ -211,10 +248,39 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Row table of packed group g (chunk-local; -1: every row absent): row r of
+// the tile is query row r of the window that starts at the group's first
+// q_start; a row inside member b at position i sees keys [0, last] of b (there
+// is no window where groups are packed: last = kv_len - 1, or the diagonal i +
+// shift under a causal type), shifted by b's kv_start past the group's first.
+// A row with no visible key gets last < first.  One full warp.
+__device__ __forceinline__ void ws_fill_rows(uint32_t* tab, const SchedSmem& s, int g, int lane) {
+  uint32_t v[kTileM / 32];
+#pragma unroll
+  for (int k = 0; k < kTileM / 32; ++k) v[k] = kRowAbsentKeys;
+  if (g >= 0) {
+    const int a = s.grp.start[g], e = s.grp.end[g];
+    const int4 f = s.span[a];
+    for (int b = a; b < e; ++b) {
+      const int4 sp = s.span[b];   // q_start, q_len, kv_start, kv_len (at most 128 each)
+      const int code = s.code[b];
+      const int r0 = sp.x - f.x, kofs = sp.z - f.z;
+      const int diag = code == kMaskPadding ? kBlockN : (code == kMaskCausalBottomRight ? sp.w - sp.y : 0);
+#pragma unroll
+      for (int k = 0; k < kTileM / 32; ++k) {
+        const int i = lane + 32 * k - r0;
+        if (i >= 0 && i < sp.y) v[k] = row_keys(kofs, kofs + min(i + diag, sp.w - 1));
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kTileM / 32; ++k) tab[lane + 32 * k] = v[k];
+}
+
 // ---------------------------------------------------------------------------
 // warp 0: scheduler + TMA producer
 // ---------------------------------------------------------------------------
-template <int DP, bool kWin>
+template <int DP, bool kWin, bool kPack>
 __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                             const CUtensorMap* tm_v, volatile uint32_t* abort_flag) {
   constexpr uint32_t kTileBytes = WsSmem<DP>::kTileBytes;
@@ -226,9 +292,24 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   Claimer claimer{0ull, 0};
   for (;;) {
     const unsigned long long w = claim_item(claimer, p);
-    WsUnit u = ws_decode<kWin>(sm.sched, p, w);
+    WsUnit u = ws_decode<kWin, kPack>(sm.sched, p, w);
     const int slot = it_cnt & 1;
-    if (lane == 0) {
+    if (kPack && u.valid && u.packed) {
+      // packed tiles: the row tables go with the unit (the slot is free once its
+      // previous unit was read)
+      if (lane == 0 && it_cnt >= 2) ok = WS_WAIT(&sm.item_empty[slot], ((it_cnt >> 1) - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) ws_fill_rows(sm.rows[slot][t], sm.sched, u.g[t], lane);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (!ok) u.valid = 0;
+        sm.items[slot] = u;
+        mbar_arrive(&sm.item_full[slot]);
+      }
+    } else if (lane == 0) {
       if (it_cnt >= 2) ok = WS_WAIT(&sm.item_empty[slot], ((it_cnt >> 1) - 1) & 1);
       if (!ok) u.valid = 0;
       sm.items[slot] = u;
@@ -632,10 +713,113 @@ __device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams
   return true;
 }
 
+// One packed tile (a group of short sequences, one KV tile): S from TMEM, each
+// row masked to its band [first, last] from the row table, softmax over the one
+// tile (the same arithmetic as a sequence's first KV tile), P back over S in two
+// halves of 64 keys, then the epilogue.  Rows of no sequence of the group
+// (first = kRowAbsent) write nothing.  Returns false when a wait gave up.
+template <typename DT, int DP>
+__device__ __forceinline__ bool ws_packed_tile(WsSmem<DP>& sm, const AttnParams& p, volatile uint32_t* abort_flag,
+                                               uint32_t tS, uint32_t tO, int tile, const WsTile& tt, uint32_t rk,
+                                               int row, float sl2, uint32_t& s_cnt, uint32_t& o_cnt) {
+  using Tr = DTypeTraits<DT>;
+  const int lane = threadIdx.x & 31;
+  const int first_raw = (int)(int16_t)(rk & 0xFFFFu);
+  const bool row_ok = first_raw != kRowAbsent;
+  const int first = row_ok ? first_raw : 0;
+  const int last = (int)(int16_t)(rk >> 16);   // < first when the row sees no key
+  float m = -INFINITY;
+  float2 lr_a = make_float2(0.f, 0.f), lr_b = lr_a, le_a = lr_a, le_b = lr_a;
+  if (tt.n > 0) {
+    if (!WS_WAIT_WARP(&sm.s_full[tile], s_cnt & 1)) return false;
+    ++s_cnt;
+    tc_fence_after();
+    uint32_t sr[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
+    tmem_ld_wait_regs32(sr);
+    tmem_tie_regs32(sr + 32);
+    tmem_tie_regs32(sr + 64);
+    tmem_tie_regs32(sr + 96);
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c > last || c < first) sr[c] = __float_as_uint(-INFINITY);
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 128; c += 8) {
+      mx0 = fmax3f(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+      mx1 = fmax3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+      mx2 = fmax3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+      mx3 = fmax3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+    }
+    m = fmax3f(fmaxf(mx0, mx1), mx2, mx3);
+    const float mb = (m == -INFINITY ? 0.f : m) * sl2;
+    const float2 scale2 = make_float2(sl2, sl2);
+    const float2 bias2 = make_float2(-mb, -mb);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      if (half == 1 && __all_sync(0xffffffffu, last < 64)) {
+        // no row of the warp sees keys 64..127: their P is zero
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        tmem_st16(tS + 32, pk);
+        tmem_st16(tS + 48, pk);
+      } else {
+#pragma unroll
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
+          uint32_t pk[16];
+          ws_exp_chunk<DT>(sr + 32 * c, pk, scale2, bias2, lr_a, lr_b, le_a, le_b);
+          tmem_st16(tS + 16 * c, pk);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(half == 0 ? &sm.p_lo[tile] : &sm.p_hi[tile]);
+    }
+    ++o_cnt;
+  }
+  // ---- epilogue ----
+  const SeqInfo& s = tt.seq;   // q_start: the group's first row
+  DT* dst = static_cast<DT*>(p.out) + ((size_t)(s.q_start + (row_ok ? row : 0)) * p.Hq + tt.h) * (size_t)p.d;
+  if (tt.n > 0) {
+    if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt - 1) & 1)) return false;
+    tc_fence_after();
+    const float l_r = (lr_a.x + lr_a.y) + (lr_b.x + lr_b.y);
+    const float l_e = (le_a.x + le_a.y) + (le_b.x + le_b.y);
+    const float inv = l_r > 0.f ? 1.f / l_r : 0.f;   // a row that saw no key stays 0
+#pragma unroll
+    for (int c = 0; c < DP / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + 32 * c, o);
+      tmem_ld_wait_regs32(o);
+      if (row_ok) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 v4;
+          v4.x = Tr::pack2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+          v4.y = Tr::pack2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+          v4.z = Tr::pack2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+          v4.w = Tr::pack2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + 32 * c + e) = v4;
+        }
+      }
+    }
+    if (row_ok && p.lse) p.lse[(size_t)tt.h * p.T + s.q_start + row] = m * p.scale + logf(l_e);
+  } else if (row_ok) {
+#pragma unroll
+    for (int col = 0; col < DP; col += 8) *reinterpret_cast<uint4*>(dst + col) = make_uint4(0u, 0u, 0u, 0u);
+    if (p.lse) p.lse[(size_t)tt.h * p.T + s.q_start + row] = -INFINITY;
+  }
+  tc_fence_before();
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // warps 2-9: softmax + epilogue, tile = (warp - 2) / 4
 // ---------------------------------------------------------------------------
-template <typename DT, int DP, bool kWin>
+template <typename DT, int DP, bool kWin, bool kPack>
 __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, int tile,
                            volatile uint32_t* abort_flag) {
   using Tr = DTypeTraits<DT>;
@@ -652,6 +836,15 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
     const int slot = it_cnt & 1;
     if (!WS_WAIT_WARP(&sm.item_full[slot], (it_cnt >> 1) & 1)) break;
     const int valid = sm.items[slot].valid;
+    if (kPack && valid && sm.items[slot].packed) {   // a packed tile: its own path
+      const WsTile tp = sm.items[slot].t[tile];
+      const uint32_t rk = sm.rows[slot][tile][row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
+      ++it_cnt;
+      if (!ws_packed_tile<DT, DP>(sm, p, abort_flag, tS, tO, tile, tp, rk, row, sl2, s_cnt, o_cnt)) break;
+      continue;
+    }
     const WsTile tt = sm.items[slot].t[tile];
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
@@ -725,10 +918,11 @@ __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, i
   }
 }
 
-template <typename DT, int DP, bool kWin>
+template <typename DT, int DP, bool kWin, bool kPack>
 __global__ void __launch_bounds__(kWsThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  static_assert(!(kWin && kPack), "short sequences are packed only without a window");
   extern __shared__ uint8_t smem_raw[];
   WsSmem<DP>& sm = *reinterpret_cast<WsSmem<DP>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -772,13 +966,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   volatile uint32_t* abort_flag = &sm.abort;
 
   if (warp == 0) {
-    ws_producer<DP, kWin>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
+    ws_producer<DP, kWin, kPack>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
   } else if (warp == 1) {
     if (lane == 0) ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
     __syncwarp();
   } else {
     zero_pad_rows(p, 64, kWsThreads - 64, 2);
-    ws_softmax<DT, DP, kWin>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
+    ws_softmax<DT, DP, kWin, kPack>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
   }
 
   tc_fence_before();

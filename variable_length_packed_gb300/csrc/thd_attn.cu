@@ -114,12 +114,21 @@ int launch_serial(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 constexpr size_t kOneCtaPerSmSmem = 120 * 1024;
 size_t one_cta_per_sm(size_t bytes) { return bytes > kOneCtaPerSmSmem ? bytes : kOneCtaPerSmSmem; }
 
+// Batches whose max_seqlen hint is at most this many rows run the instantiation
+// that packs runs of short sequences into shared tiles.  The hint only picks the
+// instantiation (both are exact for any lengths); the two compute short sequences
+// in differently laid-out tiles, so their results agree within rounding, not bit
+// for bit.
+constexpr int kPackMaxSeqlen = 256;
+
 template <typename DT, int DP>
 int launch_ws(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const thd::AttnParams& p,
-              int grid, cudaStream_t stream) {
+              int max_seqlen, int grid, cudaStream_t stream) {
   // the windowed instantiation carries the window's lower bound through the pipeline
   const bool win = p.win_left >= 0 || p.win_right >= 0;
-  auto kern = win ? thd::attn_fwd_ws_kernel<DT, DP, true> : thd::attn_fwd_ws_kernel<DT, DP, false>;
+  const bool pack = !win && max_seqlen > 0 && max_seqlen <= kPackMaxSeqlen;
+  auto kern = win ? thd::attn_fwd_ws_kernel<DT, DP, true, false>
+                  : (pack ? thd::attn_fwd_ws_kernel<DT, DP, false, true> : thd::attn_fwd_ws_kernel<DT, DP, false, false>);
   const size_t smem = one_cta_per_sm(sizeof(thd::WsSmem<DP>) + 1024);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return THD_ERR_CUDA;
@@ -387,13 +396,13 @@ int thd_attn_fwd_window(const void* q, const void* k, const void* v, const int32
   }
   const int grid = sms;
   if (bf16) {
-    if (head_dim == 128) return launch_ws<__nv_bfloat16, 128>(mq, mk, mv, p, grid, st);
-    if (head_dim == 64) return launch_ws<__nv_bfloat16, 64>(mq, mk, mv, p, grid, st);
+    if (head_dim == 128) return launch_ws<__nv_bfloat16, 128>(mq, mk, mv, p, max_seqlen, grid, st);
+    if (head_dim == 64) return launch_ws<__nv_bfloat16, 64>(mq, mk, mv, p, max_seqlen, grid, st);
     if (head_dim < 64) return launch_serial<__nv_bfloat16, 64, false>(mq, mk, mv, p, grid, st);
     return launch_serial<__nv_bfloat16, 128, false>(mq, mk, mv, p, grid, st);
   } else {
-    if (head_dim == 128) return launch_ws<__half, 128>(mq, mk, mv, p, grid, st);
-    if (head_dim == 64) return launch_ws<__half, 64>(mq, mk, mv, p, grid, st);
+    if (head_dim == 128) return launch_ws<__half, 128>(mq, mk, mv, p, max_seqlen, grid, st);
+    if (head_dim == 64) return launch_ws<__half, 64>(mq, mk, mv, p, max_seqlen, grid, st);
     if (head_dim < 64) return launch_serial<__half, 64, false>(mq, mk, mv, p, grid, st);
     return launch_serial<__half, 128, false>(mq, mk, mv, p, grid, st);
   }
