@@ -134,6 +134,9 @@ struct BwdSmem {
   alignas(1024) uint8_t q[kTileBytes];
   alignas(1024) uint8_t dout[kTileBytes];
   alignas(1024) uint8_t ds[kTileM * kTileM * 2];   // dS^T: 128 key rows x 128 queries, two 64-query panels
+  // head_dim 128: staging of the second 64 dQ columns (fp32, two 32-column panels),
+  // so that the next query tile's Q / dO can load while the dQ tile goes out
+  alignas(1024) uint8_t stage[DP > 64 ? kTileM * 64 * 4 : 1024];
   float lse2[kTileM];                              // LSE * log2(e) of the tile's queries
   float dd[kTileM];                                // D of the tile's queries
   uint64_t bar_kv, bar_q, bar_mma;
@@ -142,6 +145,10 @@ struct BwdSmem {
   WorkItem item;
   SchedSmem sched;
 };
+
+// plus up to 1 KB to align the dynamic shared memory: within the 227 KB a CTA may use
+static_assert(sizeof(BwdSmem<64>) + 1024 <= 227 * 1024 && sizeof(BwdSmem<128>) + 1024 <= 227 * 1024,
+              "shared memory of the backward kernel");
 
 constexpr int kBwdThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lanes, split the columns
 
@@ -241,7 +248,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_2d(sm.k + pn * 16384, &tm_k, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
         tma_load_2d(sm.v + pn * 16384, &tm_v, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
       }
-      bulk_wait_group_read0();   // the previous item's last dQ staging (in dO) was read
       load_q(g * p.group, s.q_start + qt_first * kTileM);   // the item's first query tile
     }
     bool first = true;
@@ -267,7 +273,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           sm.lse2[tid] = nl2;
           sm.dd[tid] = ndd;
         }
-        if (tid == 0) bulk_wait_group_read0();   // the previous tile's dQ staging was read
         __syncthreads();
         // ---- S^T = K Q^T, dP^T = V dO^T ----
         if (tid == 0) {
@@ -286,11 +291,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_ss(tDP, smem_desc_join(v_K + off, hi), smem_desc_join(o_K + off, hi), idesc_s, kk > 0 ? 1u : 0u);
           }
           umma_commit(&sm.bar_mma);
+          // the previous tile's dQ staging (in the dS^T and staging buffers) was read
+          // while these MMAs run; the barrier below orders it before the dS^T writes
+          bulk_wait_group_read0();
         }
         if (first) ph_kv ^= 1u;
         ph_q ^= 1u;
         mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
         ph_mma ^= 1u;
+        __syncthreads();
         tc_fence_after();
 
         if (tid < kTileM) {   // the next tile's statistics load while this one computes
@@ -364,13 +373,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ph_mma ^= 1u;
         tc_fence_after();
         first = false;
+        // The MMAs that read Q and dO are complete: the next query tile of the item loads
+        // while this tile's dQ goes out.
+        if (tid == 0 && !*abort_flag) {
+          const bool more = qt + 1 < nqt || hh + 1 < p.group;
+          if (more) {
+            const int nh = qt + 1 < nqt ? h : h + 1;
+            const int nrow = s.q_start + (qt + 1 < nqt ? (qt + 1) * kTileM : qt_first * kTileM);
+            load_q(nh, nrow);
+          }
+        }
         // ---- dQ tile into the fp32 accumulator by bulk tensor reductions, 64 columns
-        // at a time, staged in buffers free once the MMAs completed: the dS^T buffer,
-        // then (head_dim 128) the dO buffer ----
+        // at a time, staged in the dS^T buffer (free once the MMAs completed) and, with
+        // head_dim 128, the staging buffer ----
 #pragma unroll
         for (int r = 0; r < DP / 64; ++r) {
           const int c = 2 * r + half;   // 32-column chunk: panel `half` of the staging buffer
-          uint8_t* stage = r == 0 ? sm.ds : sm.dout;
+          uint8_t* stage = r == 0 ? sm.ds : sm.stage;
           uint32_t o[32];
           tmem_ld32(tS + t_lane + 32 * c, o);
           tmem_ld_wait_regs32(o);
@@ -387,18 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bulk_commit_group();
           }
         }
-        // The next query tile of the item loads while this tile's dQ goes out; its dO
-        // lands in a staging buffer only once the reductions have read it.  (The dS^T
-        // buffer's read is waited for before the next tile writes dS^T.)
-        if (tid == 0 && !*abort_flag) {
-          const bool more = qt + 1 < nqt || hh + 1 < p.group;
-          if (more) {
-            const int nh = qt + 1 < nqt ? h : h + 1;
-            const int nrow = s.q_start + (qt + 1 < nqt ? (qt + 1) * kTileM : qt_first * kTileM);
-            if (DP > 64) bulk_wait_group_read0();
-            load_q(nh, nrow);
-          }
-        }
+        // (the staging buffers' reads are waited for before the next tile writes dS^T)
         tc_fence_before();
         if (__syncthreads_or(*abort_flag != 0u)) {
           stop = true;
