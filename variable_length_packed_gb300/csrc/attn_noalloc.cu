@@ -61,7 +61,7 @@ extern "C" int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                     int batch_size, int max_seqlen, float softmax_scale, void* out, float* lse,
                                     int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
                                     int dtype, void* stream) {
-  // the workspace this build needs must fit the fixed buffer
+  // the workspace the library needs must fit the fixed buffer
   if (thd_attn_workspace_size() > kNoAllocScratchBytes) return THD_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int st = scratch_for_current_device(&scratch);
