@@ -323,19 +323,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait_regs32(sr);
           tmem_tie_regs32(dr);
           uint32_t pp[16], pd[16];
+          if (__all_sync(0xffffffffu, kvalid && c_lo <= 32 * c0 && c_hi >= 32 * c0 + 31)) {
+            // every key row of the warp sees all 32 queries of the chunk: no select
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pv[2], dsv[2];
+            for (int e = 0; e < 16; ++e) {
+              float pv[2], dsv[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int c = 32 * c0 + 2 * e + u;
-              const bool vis = kvalid && c >= c_lo && c <= c_hi;
-              const float x = ex2_approx(fmaf(__uint_as_float(sr[2 * e + u]), sl2, -sm.lse2[c]));
-              pv[u] = vis ? x : 0.f;
-              dsv[u] = pv[u] * (__uint_as_float(dr[2 * e + u]) - sm.dd[c]);
+              for (int u = 0; u < 2; ++u) {
+                const int c = 32 * c0 + 2 * e + u;
+                pv[u] = ex2_approx(fmaf(__uint_as_float(sr[2 * e + u]), sl2, -sm.lse2[c]));
+                dsv[u] = pv[u] * (__uint_as_float(dr[2 * e + u]) - sm.dd[c]);
+              }
+              pp[e] = Tr::pack2(pv[0], pv[1]);
+              pd[e] = Tr::pack2(dsv[0], dsv[1]);
             }
-            pp[e] = Tr::pack2(pv[0], pv[1]);
-            pd[e] = Tr::pack2(dsv[0], dsv[1]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float pv[2], dsv[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int c = 32 * c0 + 2 * e + u;
+                const bool vis = kvalid && c >= c_lo && c <= c_hi;
+                const float x = ex2_approx(fmaf(__uint_as_float(sr[2 * e + u]), sl2, -sm.lse2[c]));
+                pv[u] = vis ? x : 0.f;
+                dsv[u] = pv[u] * (__uint_as_float(dr[2 * e + u]) - sm.dd[c]);
+              }
+              pp[e] = Tr::pack2(pv[0], pv[1]);
+              pd[e] = Tr::pack2(dsv[0], dsv[1]);
+            }
           }
           // P^T / dS^T of these 32 queries over the first 16 of their own 32 S^T / dP^T
           // columns: the other column half may still be reading its chunks
