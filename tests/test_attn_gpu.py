@@ -290,7 +290,8 @@ def test_garbage_past_batch_is_ignored_and_deterministic():
     compare_full(w, out1, lse1)
 
 
-def test_writes_stay_inside_out_and_lse():
+@pytest.mark.parametrize("hint", [140, 4096])   # the packing and the plain instantiation
+def test_writes_stay_inside_out_and_lse(hint):
     w = workloads.from_lengths("guard", [33, 140], [1, 0], gaps_before=[2, 5], trailing=4, heads_q=2,
                                head_dim=64, dtype=torch.bfloat16, seed=14)
     dev = to_device(w)
@@ -301,25 +302,33 @@ def test_writes_stay_inside_out_and_lse():
     out = obuf[g:g + T]
     lse = lbuf[1024:1024 + H * T].view(H, T)
     vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"], dev["padded"],
-                     dev["causal"], w.batch_size, w.max_seqlen, w.softmax_scale, out=out, lse=lse)
+                     dev["causal"], w.batch_size, hint, w.softmax_scale, out=out, lse=lse)
     torch.cuda.synchronize()
     assert torch.all(obuf[:g] == 3.0) and torch.all(obuf[g + T:] == 3.0)
     assert torch.all(lbuf[:1024] == 5.0) and torch.all(lbuf[1024 + H * T:] == 5.0)
     compare_full(w, out, lse)
 
 
-def test_non_monotone_metadata_does_not_fault():
-    """Invalid device metadata: unspecified output, but the call completes without a fault."""
+@pytest.mark.parametrize("hint", [40, 4096])   # the packing and the plain instantiation
+def test_non_monotone_metadata_does_not_fault(hint):
+    """Invalid device metadata: unspecified output, but the call completes without a fault.
+    Also short sequences whose rows overlap (a later one starting before an earlier one
+    ends), which the packing must not put in one tile."""
     w = workloads.from_lengths("bad", [40, 40, 40], [1, 0, 1], heads_q=2, head_dim=64, dtype=torch.bfloat16,
                                seed=15)
     dev = to_device(w)
-    bad_cu = torch.tensor([0, 100, 20, 10000], dtype=torch.int32, device="cuda")
-    bad_pad = torch.tensor([-50, 90, 119, 3], dtype=torch.int32, device="cuda")
-    ws = workspace()
-    vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], bad_cu, bad_cu, bad_pad, bad_pad, dev["causal"], 3, 40,
-                     0.125, workspace=ws)
-    torch.cuda.synchronize()
-    assert status_word(ws) == 0
+    cases = [([0, 100, 20, 10000], [-50, 90, 119, 3], dev["causal"]),
+             ([0, 10, 20, 30], [5, 0, 3, 30], dev["causal"]),
+             ([0, 30, 31, 60], [60, 100, 90, 120], dev["causal"]),
+             (list(range(0, 45, 5)), [0, 5, 10, 15, 12, 20, 30, 35, 40], None)]
+    for cu, pad, causal in cases:
+        bad_cu = torch.tensor(cu, dtype=torch.int32, device="cuda")
+        bad_pad = torch.tensor(pad, dtype=torch.int32, device="cuda")
+        ws = workspace()
+        vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], bad_cu, bad_cu, bad_pad, bad_pad, causal, len(cu) - 1, hint,
+                         0.125, workspace=ws)
+        torch.cuda.synchronize()
+        assert status_word(ws) == 0
 
 
 def test_max_seqlen_hint_picks_the_layout_not_the_result():
