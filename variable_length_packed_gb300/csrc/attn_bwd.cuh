@@ -23,7 +23,7 @@
 //   post  dQ = scale * accumulator, rounded to the input type.
 // head_dim 64 or 128 (TMA loads).  Eight warps: warps w and w + 4 read the
 // same TMEM lanes and split the columns of the elementwise step, the dQ
-// atomics and the dK / dV epilogue; the next query tile's Q and dO load while
+// staging and the dK / dV epilogue; the next query tile's Q and dO load while
 // the current tile's dQ is added.
 #pragma once
 #include "attn_common.cuh"

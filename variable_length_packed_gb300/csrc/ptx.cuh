@@ -309,16 +309,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ----------------------------------------------------------------------------
-// global reductions
-// ----------------------------------------------------------------------------
-// dst[0..3] += v, four fp32 adds in one reduction without a returned value
-// (the issuing thread does not wait for it).
-__device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
-}
-
-// ----------------------------------------------------------------------------
 // math helpers
 // ----------------------------------------------------------------------------
 // max of three floats in one instruction (PTX max.f32 with three sources).
