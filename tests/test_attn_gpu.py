@@ -221,6 +221,39 @@ def test_packed_tiles_of_tiny_sequences(d, dtype):
     assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
 
 
+def test_packed_groups_without_keys():
+    """Packed groups whose sequences have no keys at all (the tile visits no KV tile), next
+    to groups that have some: rows without keys are exact zeros with -inf LSE."""
+    lq = np.array([5, 7, 3, 9, 2, 4, 6, 1], dtype=np.int64)
+    lkv = np.array([0, 0, 0, 0, 3, 4, 0, 2], dtype=np.int64)
+    codes = np.array([0, 1, 2, 0, 1, 2, 0, 0], dtype=np.uint8)
+    q_starts = np.concatenate([[0], np.cumsum(lq)[:-1]]).astype(np.int32)
+    q_starts[4:] += 200   # a second run, in another group
+    kv_starts = np.concatenate([[0], np.cumsum(lkv)[:-1]]).astype(np.int32) + 50
+    B = len(lq)
+    T = int(max(q_starts[-1] + lq[-1], kv_starts[-1] + lkv[-1]) + 3)
+    w = workloads.from_lengths("nokeys", [T], [0], heads_q=2, heads_kv=1, head_dim=64, dtype=torch.bfloat16,
+                               seed=41)
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    ws = workspace()
+    out, lse = vlp.thd_attn_fwd(w.q.cuda(), w.k.cuda(), w.v.cuda(), dev(cu_q), dev(cu_k), dev(q_starts),
+                                dev(kv_starts), dev(codes), B, 16, w.softmax_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert status_word(ws) == 0
+    ref, ref_lse = oracle.thd_attention_fwd_general(w.q, w.k, w.v, cu_q, cu_k, q_starts, kv_starts, codes, B,
+                                                    w.softmax_scale)
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    seen = np.isfinite(ref_lse)
+    assert_out_close(o, ref, torch.bfloat16, "no keys")
+    assert np.array_equal(np.isfinite(l), seen)
+    assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
+    assert np.all(o[:, :, :][~seen.any(axis=0)] == 0.0)
+    assert (~seen[:, q_starts[0]:q_starts[3] + lq[3]]).all()   # the first run sees no key
+
+
 def test_packing_is_decided_per_chunk():
     """One launch, two scheduler chunks: in the first, every short sequence is followed by a
     long one (nothing to pack: one tile per (sequence, head)); in the second, runs of tiny
