@@ -92,8 +92,10 @@ def kernel_sources_sha(kind):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kind):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current sources."""
+def recorded_traffic(kind, workload=None):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current sources
+    and the workload: the captured workload's own figure, the scaled figure for the workload
+    it was scaled to, None for any other workload."""
     path = os.path.join(ROOT, "profiles", f"{kind}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -105,10 +107,17 @@ def recorded_traffic(kind):
                 vals[k.strip()] = v.strip()
     if vals.get("kernel_sources_sha256") != kernel_sources_sha(kind):
         return None
+    captured, _, scaled = vals.get("workload", "").partition("->")
+    captured = captured.strip()
+    scaled = scaled.split("(")[0].strip() or captured
     try:
-        return float(vals["dram_bytes_per_launch_full_workload"])
+        if workload is None or workload == scaled:
+            return float(vals["dram_bytes_per_launch_full_workload"])
+        if workload == captured:
+            return float(vals["dram_bytes_per_launch_capture"])
     except (KeyError, ValueError):
         return None
+    return None
 
 
 class ClockSampler:
@@ -536,7 +545,7 @@ def run_gpu(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
         "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": recorded_traffic("attn_fwd"),
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": recorded_traffic("attn_fwd", args.workload),
                      "kernel": "thd attention forward", "peak_source": f"{peak_src} bf16 dense (burst)",
                      "frac_of_sustained_peak": achieved / peaks["bf16_tflops_sustained"],
                      "attn_ms_per_launch": attn_ms, "algorithmic_flops_per_launch": eff,

@@ -85,3 +85,17 @@ def test_reference_arm_prints_oracle_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["warmup"] >= 3
+
+
+def test_recorded_traffic_follows_the_workload():
+    """The committed DRAM record applies to the workload it was captured on (its own figure)
+    and to the one it was scaled to; any other workload reports no traffic."""
+    import bench
+    full = bench.recorded_traffic("attn_fwd", "long_context")
+    small = bench.recorded_traffic("attn_fwd", "long_context_small")
+    if full is None:   # the record no longer matches the kernel sources
+        assert small is None
+        return
+    assert small is not None and abs(full - 4 * small) < 1.0
+    assert bench.recorded_traffic("attn_fwd", "many_short") is None
+    assert bench.recorded_traffic("attn_fwd") == full
