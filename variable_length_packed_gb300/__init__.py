@@ -140,6 +140,8 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     per-sequence mask type: MASK_PADDING (0), MASK_PADDING_CAUSAL (1, top-left) or
     MASK_PADDING_CAUSAL_BOTTOM_RIGHT (2).  q and k/v sequences may differ in length.
     window: (left, right) sliding window around the mask type's diagonal, -1 = unbounded.
+    max_seqlen: a hint (never trusted for correctness); 1..256 selects the kernel that packs
+    runs of short sequences into shared tiles (see thd_attn_fwd in include/thd_attn.h).
     Returns (out [T, Hq, d], lse [Hq, T] float32 or None).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
