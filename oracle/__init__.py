@@ -26,7 +26,8 @@ Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 case counts).  Nothing is "parity unpinned".
 """
 from .attention import (thd_attention_fwd, thd_attention_rows, sequence_spans, thd_attention_fwd_general,
-                        merge_partials, visible_keys, visible_range, thd_attention_bwd, MASK_PADDING,
+                        merge_partials, visible_keys, visible_range, thd_attention_bwd,
+                        thd_attention_bwd_dq_rows, MASK_PADDING,
                         MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT)
 from .mask import (padding_mask_loop, padding_mask_formula, padding_mask_cross_loop,
                    padding_mask_cross_formula)
@@ -34,6 +35,7 @@ from .mask import (padding_mask_loop, padding_mask_formula, padding_mask_cross_l
 __all__ = [
     "thd_attention_fwd",
     "thd_attention_rows",
+    "thd_attention_bwd_dq_rows",
     "sequence_spans",
     "thd_attention_fwd_general",
     "merge_partials",

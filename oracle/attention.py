@@ -298,3 +298,31 @@ def thd_attention_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_p
             dk[sk, g, :] += softmax_scale * (dZ.T @ Q)
             dv[sk, g, :] += P.T @ dO
     return dq, dk, dv
+
+
+def thd_attention_bwd_dq_rows(q, k, v, dout, start_q, start_kv, length, causal, head, group,
+                              softmax_scale, row_ids):
+    """dQ of selected query rows of one (sequence, head), for full-size batches checked on
+    sampled rows: the gradient of ``thd_attention_rows``'s output, written out row by row from
+    the same chain rule as ``thd_attention_bwd`` (a query row's dQ depends on that row and on
+    the sequence's keys and values only):
+
+        z_j = scale q_i . k_j (visible j),  p = softmax(z),  dp_j = dO_i . v_j,
+        dz_j = p_j (dp_j - sum_l p_l dp_l),  dQ_i = scale sum_j dz_j k_j.
+
+    ``row_ids`` are positions inside the sequence; returns dq [n, d] in fp64.
+    """
+    g = head // group
+    rows = np.asarray(row_ids, dtype=np.int64)
+    qq = _as64(q[start_q + rows, head, :])
+    oo = _as64(dout[start_q + rows, head, :])
+    kk = _as64(k[start_kv:start_kv + length, g, :])
+    vv = _as64(v[start_kv:start_kv + length, g, :])
+    z = softmax_scale * (qq @ kk.T)
+    if causal:
+        z = np.where(np.arange(length)[None, :] <= rows[:, None], z, -np.inf)
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    p = e / e.sum(axis=1, keepdims=True)
+    dp = oo @ vv.T
+    dz = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    return softmax_scale * (dz @ kk)

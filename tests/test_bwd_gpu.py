@@ -131,3 +131,30 @@ def test_mixed_gqa_sampled_sequences():
         check(w, (dq[sub], dk[sub], dv[sub]), ref, f"gqa b={b} L={L}")
     pad = torch.from_numpy(~valid_rows(w)).cuda()
     assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
+
+
+def test_long_context_backward_sampled_dq_rows():
+    """The full-size long-context batch in the configuration bench.py times (its own
+    max_seqlen hint): dQ of sampled rows (tile edges and random rows) of two heads of every
+    sequence against the row-wise fp64 oracle.  (dK / dV need every query row of a sequence;
+    they are checked element by element on the smaller batches above.)"""
+    w = workloads.make("long_context")
+    dev = to_device(w)
+    out, lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"], dev["padded"],
+                                dev["causal"], w.batch_size, w.max_seqlen, w.softmax_scale)
+    dout = workloads.grad_output(w, 7)
+    dq, _, _ = vlp.thd_attn_bwd(dev["q"], dev["k"], dev["v"], out, lse, dout.cuda(), dev["cu"], dev["cu"],
+                                dev["padded"], dev["padded"], dev["causal"], w.batch_size, w.max_seqlen,
+                                w.softmax_scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(77)
+    group = w.num_heads_q // w.num_heads_kv
+    for b in range(w.batch_size):
+        s, L = int(w.starts[b]), int(w.lengths[b])
+        for h in rng.choice(w.num_heads_q, size=2, replace=False):
+            rows = np.unique(np.r_[0, 1, 127, 128, L - 129, L - 1, rng.integers(0, L, 6)])
+            ref = oracle.thd_attention_bwd_dq_rows(w.q, w.k, w.v, dout, s, s, L, bool(w.causal[b]), int(h), group,
+                                                   w.softmax_scale, rows)
+            got = dq[s + torch.from_numpy(rows).cuda(), int(h)].float().cpu().double().numpy()
+            err = np.abs(got - ref).max()
+            assert err <= REL[w.dtype] * np.abs(ref).max(), (b, int(h), err, np.abs(ref).max())

@@ -112,3 +112,23 @@ def test_mixed_policy_gradients_equal_per_sequence():
         np.testing.assert_allclose(dq[sub], g1[0], atol=1e-14)
         np.testing.assert_allclose(dk[sub], g1[1], atol=1e-14)
         np.testing.assert_allclose(dv[sub], g1[2], atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dq_rows_against_torch_autograd(causal):
+    """The row-wise dQ used to check full-size batches on sampled rows equals torch fp64
+    autograd through scaled_dot_product_attention on those rows (grouped heads, a sequence
+    inside a packed buffer)."""
+    w = workloads.from_lengths("bwr", [5, 37], [causal, causal], gaps_before=[1, 4], trailing=3, heads_q=4,
+                               heads_kv=2, head_dim=16, seed=61)
+    dout = _dout(w, 62)
+    s, L = int(w.starts[1]), int(w.lengths[1])
+    rows = np.array([0, 1, 17, L - 2, L - 1])
+    q = w.q[s:s + L].double().transpose(0, 1).clone().requires_grad_()
+    kk = w.k[s:s + L].double().transpose(0, 1).repeat_interleave(2, dim=0)
+    vv = w.v[s:s + L].double().transpose(0, 1).repeat_interleave(2, dim=0)
+    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=causal, scale=w.softmax_scale)
+    o.backward(dout[s:s + L].double().transpose(0, 1))
+    for h in range(4):
+        got = oracle.thd_attention_bwd_dq_rows(w.q, w.k, w.v, dout, s, s, L, causal, h, 2, w.softmax_scale, rows)
+        np.testing.assert_allclose(got, q.grad[h, rows].numpy(), atol=1e-12)
