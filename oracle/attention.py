@@ -113,12 +113,14 @@ def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
 
 
 def thd_attention_rows(q, k, v, start_q, start_kv, length, causal, head, group,
-                       softmax_scale, row_ids):
+                       softmax_scale, row_ids, window=(-1, -1)):
     """Oracle values for selected query rows of one (sequence, head).
 
     Used to check full-size batches on sampled rows.  ``row_ids`` are positions
     inside the sequence (0-based).  ``q``/``k``/``v`` are the full packed
-    tensors (torch or numpy).  Returns (out [n, d], lse [n]) in fp64.
+    tensors (torch or numpy).  ``window``: (left, right) as in ``visible_range``
+    (top-left causal or full, equal query and key lengths).  Returns
+    (out [n, d], lse [n]) in fp64.
     """
     g = head // group
     rows = np.asarray(row_ids, dtype=np.int64)
@@ -126,7 +128,12 @@ def thd_attention_rows(q, k, v, start_q, start_kv, length, causal, head, group,
     kk = _as64(k[start_kv:start_kv + length, g, :])
     vv = _as64(v[start_kv:start_kv + length, g, :])
     z = softmax_scale * (qq @ kk.T)
-    if causal:
+    if tuple(window) != (-1, -1):
+        code = MASK_PADDING_CAUSAL if causal else MASK_PADDING
+        band = np.array([visible_range(int(i), length, length, code, window) for i in rows])
+        keys = np.arange(length)[None, :]
+        z = np.where((keys >= band[:, :1]) & (keys < band[:, 1:]), z, -np.inf)
+    elif causal:
         z = np.where(np.arange(length)[None, :] <= rows[:, None], z, -np.inf)
     zmax = z.max(axis=1, keepdims=True)
     e = np.exp(z - zmax)

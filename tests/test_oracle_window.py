@@ -129,3 +129,21 @@ def test_window_gradients_against_autograd(code, window):
     np.testing.assert_allclose(dq, qq.grad.numpy(), atol=1e-12)
     np.testing.assert_allclose(dk, kk.grad.numpy(), atol=1e-12)
     np.testing.assert_allclose(dv, vv.grad.numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("code", [0, 1])
+@pytest.mark.parametrize("window", [(3, -1), (2, 4), (0, 0), (5, 0), (-1, -1)])
+def test_sampled_rows_with_window_against_tril_triu(code, window):
+    """The sampled-rows oracle (used on full-size batches) with a window equals the torch
+    tril / triu band on those rows, for a sequence inside a packed buffer with grouped heads."""
+    L, off = 23, 4
+    q, k, v = _rect(L + off + 3, L + off + 3, h=2, d=8, seed=code * 7 + window[0] + 3)
+    scale = 0.41
+    rows = np.array([0, 1, 9, L - 2, L - 1])
+    band = _band(L, L, code, *window)
+    kk, vv = k[:, :1].repeat(1, 2, 1), v[:, :1].repeat(1, 2, 1)   # key/value head 0 serves both query heads
+    ref, ref_lse = _torch_attention(q[off:off + L], kk[off:off + L], vv[off:off + L], band, scale)
+    for h in range(2):
+        out, lse = oracle.thd_attention_rows(q, k, v, off, off, L, code == 1, h, 2, scale, rows, window=window)
+        np.testing.assert_allclose(out, ref[rows, h].numpy(), atol=1e-12)
+        np.testing.assert_allclose(lse, ref_lse[h, rows].numpy(), atol=1e-12)

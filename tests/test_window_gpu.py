@@ -117,3 +117,27 @@ def test_window_backward_matches_oracle(d, dtype, window):
         g = g.float().cpu().double().numpy()
         scale = max(np.abs(r).max(), term if name != "dv" else 0.0)
         assert np.abs(g - r).max() <= REL[dtype] * scale + 1e-6, (name, window)
+
+
+def test_long_context_window_sampled_rows():
+    """The full-size long-context batch with the window bench.py times, (2048, 2048), in the
+    same call: sampled rows (tile and band edges, random rows) of two heads of every sequence
+    against the fp64 oracle."""
+    w = workloads.make("long_context")
+    dev = to_device(w)
+    window = (2048, 2048)
+    out, lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], None, None, dev["causal"],
+                                w.batch_size, w.max_seqlen, w.softmax_scale, window=window)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(88)
+    group = w.num_heads_q // w.num_heads_kv
+    for b in range(w.batch_size):
+        s, L = int(w.starts[b]), int(w.lengths[b])
+        edges = [0, 1, 127, 128, 2047, 2048, 2049, L - 2049, L - 2048, L - 1]
+        rows = np.unique(np.clip(np.r_[edges, rng.integers(0, L, 6)], 0, L - 1))
+        for h in rng.choice(w.num_heads_q, size=2, replace=False):
+            ref_o, ref_l = oracle.thd_attention_rows(w.q, w.k, w.v, s, s, L, bool(w.causal[b]), int(h), group,
+                                                     w.softmax_scale, rows, window=window)
+            idx = s + torch.from_numpy(rows).cuda()
+            assert_out_close(out[idx, int(h)].float().cpu().double().numpy(), ref_o, w.dtype, f"b={b} h={int(h)}")
+            assert np.abs(lse[int(h), idx].cpu().double().numpy() - ref_l).max() <= LSE_ATOL
