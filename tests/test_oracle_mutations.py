@@ -191,3 +191,66 @@ def test_window_pins_catch_mutant(monkeypatch, mutant):
         except (AssertionError, ValueError, IndexError):
             failed += 1
     assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
+
+
+# ---- the sampled-rows oracles used on full-size batches ----
+
+import test_oracle_bwd as bwd_pins
+
+
+def _dq_rows_mutant(kind):
+    def dq_rows(q, k, v, dout, start_q, start_kv, length, causal, head, group, softmax_scale, row_ids):
+        g = head // group
+        rows = np.asarray(row_ids, dtype=np.int64)
+        qq = oa._as64(q[start_q + rows, head, :])
+        oo = oa._as64(dout[start_q + rows, head, :])
+        kk = oa._as64(k[start_kv:start_kv + length, g, :])
+        vv = oa._as64(v[start_kv:start_kv + length, g, :])
+        z = softmax_scale * (qq @ kk.T)
+        if causal:
+            z = np.where(np.arange(length)[None, :] <= rows[:, None], z, -np.inf)
+        e = np.exp(z - z.max(axis=1, keepdims=True))
+        p = e / e.sum(axis=1, keepdims=True)
+        dp = oo @ vv.T
+        if kind == "no_centering":     # mistake: the softmax Jacobian's rowsum term dropped
+            dz = p * dp
+        else:
+            dz = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        if kind == "value_operand":    # mistake: dQ contracted with V instead of K
+            return softmax_scale * (dz @ vv)
+        if kind == "no_scale":         # mistake: the outer scale of dQ = scale dZ K dropped
+            return dz @ kk
+        return softmax_scale * (dz @ kk)
+    dq_rows.__name__ = f"dq_rows_{kind}"
+    return dq_rows
+
+
+@pytest.mark.parametrize("kind", ["no_centering", "value_operand", "no_scale"])
+def test_dq_rows_pin_catches_mutant(monkeypatch, kind):
+    import oracle as pkg
+    mutant = _dq_rows_mutant(kind)
+    monkeypatch.setattr(oa, "thd_attention_bwd_dq_rows", mutant)
+    monkeypatch.setattr(pkg, "thd_attention_bwd_dq_rows", mutant)
+    failed = 0
+    for causal in (False, True):
+        try:
+            bwd_pins.test_dq_rows_against_torch_autograd(causal)
+        except AssertionError:
+            failed += 1
+    assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
+
+
+@pytest.mark.parametrize("mutant", [window_lower_off_by_one, window_upper_exclusive])
+def test_windowed_rows_pin_catches_mutant(monkeypatch, mutant):
+    import oracle as pkg
+    monkeypatch.setattr(oa, "visible_range", mutant)
+    monkeypatch.setattr(pkg, "visible_range", mutant)
+    failed = 0
+    for code in (0, 1):
+        for w in ((3, -1), (2, 4), (5, 0)):
+            try:
+                with np.errstate(invalid="ignore"):   # a mutant may leave a row without keys
+                    win.test_sampled_rows_with_window_against_tril_triu(code, w)
+            except AssertionError:
+                failed += 1
+    assert failed >= 1, f"no pin caught mutant {mutant.__name__}"
