@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from thd_testutil import OUT_ATOL, assert_out_close, out_bound
+from thd_testutil import OUT_ATOL, OutErrors, assert_out_close, out_bound
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
@@ -57,3 +57,31 @@ def test_systematic_excess_fails_the_count():
     got[1:] = ref[1:] + 0.005   # one element above the flat bound is allowed
     assert_out_close(got, ref, torch.bfloat16, "single") == pytest.approx(0.012)
     assert OUT_ATOL[torch.bfloat16] == 1e-2 and OUT_ATOL[torch.float16] == 2e-3
+
+
+def test_count_is_taken_over_the_whole_sample_not_per_piece():
+    """Sampled parity gathers every (sequence, head) piece before counting: one planted
+    over-flat element in each of 600 small pieces (64 rows x 64 columns, the size of the
+    many-short batch's sampled pairs) is 600 of 2.46M elements, above the one-in-10^4
+    allowance (245), so it fails, although each piece alone would pass its own count."""
+    rng = np.random.default_rng(11)
+    acc = OutErrors(torch.bfloat16, "planted")
+    for _ in range(600):
+        ref = rng.normal(0.0, 0.5, size=(64, 64))
+        got = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        i, j = rng.integers(0, 64, size=2)
+        ref[i, j] = 3.0
+        got[i, j] = 3.0 + 0.0105   # above 1e-2, within the half-ulp allowance at 3
+        assert_out_close(got, ref, torch.bfloat16, "one piece")   # passes alone
+        acc.add(got, ref)
+    with pytest.raises(AssertionError):
+        acc.check()
+
+
+def test_whole_sample_count_passes_correctly_rounded_pieces():
+    rng = np.random.default_rng(12)
+    acc = OutErrors(torch.bfloat16, "rounded pieces")
+    for _ in range(200):
+        ref = rng.normal(0.0, 1.0, size=(37, 128))
+        acc.add(torch.from_numpy(ref).to(torch.bfloat16).double().numpy(), ref)
+    assert acc.check() < 0.0157

@@ -13,7 +13,7 @@ import torch
 import oracle
 import workloads
 from test_bwd_gpu import REL
-from thd_testutil import LSE_ATOL, assert_out_close, to_device
+from thd_testutil import LSE_ATOL, OutErrors, assert_out_close, to_device
 
 pytestmark = pytest.mark.gpu
 vlp = pytest.importorskip("variable_length_packed_gb300")
@@ -131,6 +131,7 @@ def test_long_context_window_sampled_rows():
     torch.cuda.synchronize()
     rng = np.random.default_rng(88)
     group = w.num_heads_q // w.num_heads_kv
+    acc = OutErrors(w.dtype, f"long_context window {window}")   # the count over every sampled row
     for b in range(w.batch_size):
         s, L = int(w.starts[b]), int(w.lengths[b])
         edges = [0, 1, 127, 128, 2047, 2048, 2049, L - 2049, L - 2048, L - 1]
@@ -139,5 +140,6 @@ def test_long_context_window_sampled_rows():
             ref_o, ref_l = oracle.thd_attention_rows(w.q, w.k, w.v, s, s, L, bool(w.causal[b]), int(h), group,
                                                      w.softmax_scale, rows, window=window)
             idx = s + torch.from_numpy(rows).cuda()
-            assert_out_close(out[idx, int(h)].float().cpu().double().numpy(), ref_o, w.dtype, f"b={b} h={int(h)}")
+            acc.add(out[idx, int(h)].float().cpu().double().numpy(), ref_o, f"b={b} h={int(h)}")
             assert np.abs(lse[int(h), idx].cpu().double().numpy() - ref_l).max() <= LSE_ATOL
+    acc.check()

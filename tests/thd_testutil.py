@@ -29,17 +29,45 @@ def assert_out_close(got, ref, dtype, what=""):
     """|got - ref| within out_bound everywhere, and above the flat OUT_ATOL in at most one
     element in 10^4 (so the half-ulp allowance cannot hide a systematic error).  Returns the
     largest error."""
-    got = np.asarray(got, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    err = np.abs(got - ref)
-    if err.size == 0:
-        return 0.0
-    worst = float(err.max())
-    bound = out_bound(ref, dtype)
-    assert np.all(err <= bound), f"{what}: max |out err| {worst:.3e}, above the rounding bound"
-    over = int((err > OUT_ATOL[dtype]).sum())
-    assert over <= max(1, err.size // 10000), f"{what}: {over} of {err.size} elements above {OUT_ATOL[dtype]}"
-    return worst
+    acc = OutErrors(dtype, what)
+    acc.add(got, ref)
+    return acc.check()
+
+
+class OutErrors:
+    """Output errors gathered over many samples (e.g. every sampled (sequence, head, row) of a
+    batch), checked once: each element against out_bound, and the one-in-10^4 count of
+    elements above the flat OUT_ATOL over the whole sample, not per piece, so that one
+    over-bound element per (sequence, head) cannot pass where pieces are small."""
+
+    def __init__(self, dtype, what=""):
+        self.dtype = dtype
+        self.what = what
+        self.n = 0
+        self.over = 0
+        self.worst = 0.0
+
+    def add(self, got, ref, where=""):
+        got = np.asarray(got, dtype=np.float64)
+        ref = np.asarray(ref, dtype=np.float64)
+        err = np.abs(got - ref)
+        if err.size == 0:
+            return
+        worst = float(err.max())
+        bound = out_bound(ref, self.dtype)
+        assert np.all(err <= bound), f"{self.what} {where}: max |out err| {worst:.3e}, above the rounding bound"
+        self.n += err.size
+        self.over += int((err > OUT_ATOL[self.dtype]).sum())
+        self.worst = max(self.worst, worst)
+
+    def check(self):
+        """The count over everything added; returns the largest error."""
+        allowed = max(1, self.n // 10000)
+        if self.n:
+            print(f"{self.what}: {self.over} of {self.n} elements above {OUT_ATOL[self.dtype]} "
+                  f"(allowed {allowed}), max |err| {self.worst:.3e}")
+        assert self.over <= allowed, f"{self.what}: {self.over} of {self.n} elements above {OUT_ATOL[self.dtype]}"
+        return self.worst
 
 
 def to_device(w, device="cuda"):
@@ -98,21 +126,22 @@ def compare_full(w, out, lse, ref_out=None, ref_lse=None):
 
 
 def compare_sampled(w, out, lse, pairs, rows_for):
-    """Compare selected rows of selected (sequence, head) pairs against the oracle, row by row."""
+    """Compare selected rows of selected (sequence, head) pairs against the oracle, row by row.
+    The output bound applies per element and its count over all samples together."""
     group = w.num_heads_q // w.num_heads_kv
-    worst = 0.0
+    acc = OutErrors(w.dtype, w.name)
     for b, h in pairs:
         s, L = int(w.starts[b]), int(w.lengths[b])
         rows = np.unique(np.clip(np.asarray(rows_for(L)), 0, L - 1))
         ref_o, ref_l = oracle.thd_attention_rows(w.q, w.k, w.v, s, s, L, bool(w.causal[b]), h, group,
                                                  w.softmax_scale, rows)
         got = out[s + torch.from_numpy(rows).to(out.device), h, :].float().cpu().double().numpy()
-        err = assert_out_close(got, ref_o, w.dtype, f"{w.name} b={b} h={h}")
+        acc.add(got, ref_o, f"b={b} h={h}")
         if lse is not None:
             gl = lse[h, s + torch.from_numpy(rows).to(lse.device)].cpu().double().numpy()
             lerr = np.abs(gl - ref_l).max()
             assert lerr <= LSE_ATOL, f"{w.name} b={b} h={h}: |lse err| {lerr:.3e}"
-        worst = max(worst, float(err))
+    worst = acc.check()
     check_pad_rows(w, out, lse)
     return worst
 
