@@ -229,6 +229,12 @@ int thd_attn_bwd_window(const void* q, const void* k, const void* v, const void*
  *   each call; it keeps the last call's contents.
  * - THD_ERR_WORKSPACE if the library's workspace requirement ever exceeds the
  *   fixed buffer; otherwise the same status codes as thd_attn_fwd.
+ * - A pipeline wait that gives up sets THD_STATUS_WAIT_TIMEOUT in the buffer's
+ *   status word, exactly as in thd_attn_fwd's workspace; read it with
+ *   thd_attn_noalloc_status.  The call's own return value reports only the
+ *   host-side checks and the launch.
+ * - The buffer's address is cached per device for the life of the process:
+ *   do not keep using this entry point across cudaDeviceReset.
  */
 int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
@@ -238,6 +244,20 @@ int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                          void* out, float* lse,
                          int total_tokens, int num_heads_q, int num_heads_kv, int head_dim,
                          int dtype, void* stream);
+
+/*
+ * thd_attn_noalloc_status — copies the device status word (THD_STATUS_* bits)
+ * of thd_attn_fwd_noalloc's fixed buffer on the current device to *status.
+ *
+ * No counterpart on the pages: it completes thd_attn_fwd_noalloc, whose callers
+ * hold no workspace of their own to read the status word from.  The copy is
+ * queued on `stream` after the work already queued there, and the calling host
+ * thread waits for it (this call synchronises `stream`), so it reports the last
+ * no-allocation call on this device ordered before it.  Allocates nothing.
+ * status: host pointer to one uint32.  Errors: THD_ERR_ARG (NULL status),
+ * THD_ERR_CUDA.
+ */
+int thd_attn_noalloc_status(uint32_t* status, void* stream);
 
 /*
  * thd_padding_mask — the boolean attention padding mask built on the device,
@@ -296,6 +316,23 @@ int thd_padding_mask_cross(const int32_t* cu_seqlens_q, const int32_t* cu_seqlen
 int thd_attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
                    void* out, float* lse, int total_tokens, int num_heads, int head_dim, int dtype,
                    void* stream);
+
+/*
+ * thd_set_wait_limit_ns — the time limit of one pipeline wait inside the
+ * attention kernels (forward, windowed forward, no-allocation forward,
+ * backward), for calls made after it on any host thread; returns the previous
+ * limit.  0 restores the default of 2 s.
+ *
+ * No counterpart on the pages: it belongs to the library's failure handling.
+ * Every wait of a kernel on its own pipeline (a copy landing, an MMA
+ * completing, a hand-off between warps) is bounded by this limit; a wait that
+ * runs out sets THD_STATUS_WAIT_TIMEOUT in the call's status word, the CTA
+ * stops taking work, lets the copies and MMAs it already started finish,
+ * releases its tensor memory and exits, and the call's output is unspecified.
+ * No wait is expected to come near the default; a short limit makes the waits
+ * run out on purpose, which is how the failure path itself is tested.
+ */
+uint64_t thd_set_wait_limit_ns(uint64_t ns);
 
 /* Human-readable name of a thd_status value (static storage). */
 const char* thd_status_string(int status);

@@ -143,3 +143,51 @@ def test_window_arguments_rejected_before_launch(lib):
     assert bwd(-3, 0) == -1 and bwd(2, -2) == -1
     with pytest.raises(ValueError):
         vlp._window_args((-2, 0))
+
+
+def _qkv_cpu(T=16, Hq=2, Hkv=2, d=64, dtype=None):
+    import torch
+    dtype = dtype or torch.bfloat16
+    return (torch.zeros((T, Hq, d), dtype=dtype), torch.zeros((T, Hkv, d), dtype=dtype),
+            torch.zeros((T, Hkv, d), dtype=dtype))
+
+
+@pytest.mark.parametrize("fn", ["thd_attn_fwd", "thd_attn_fwd_noalloc"])
+def test_binding_refuses_bad_qkv_before_any_launch(fn):
+    """Both forward wrappers check q/k/v shapes and dtypes, and the metadata dtypes, before
+    anything reaches the library: a k or v with fewer tokens than q (the library would read
+    past its end), a head_dim mismatch, mixed or fp32 dtypes, int64 cu_seqlens, a float
+    per-sequence flag.  The tensors here are on the CPU; each case fails on its own check,
+    ahead of the CUDA-tensor check."""
+    import torch
+    call = getattr(vlp, fn)
+    cu = torch.tensor([0, 16], dtype=torch.int32)
+
+    def run(q, k, v, cu_q=cu, flags=None):
+        if fn == "thd_attn_fwd":
+            return call(q, k, v, cu_q, cu_q, None, None, flags, 1, 16, 0.125)
+        return call(q, k, v, cu_q, cu_q, None, None, flags, 1, 16, 0.125, torch.empty_like(q))
+
+    q, k, v = _qkv_cpu()
+    with pytest.raises(ValueError, match="k and v"):
+        run(q, k[:8], v)                                # short k
+    with pytest.raises(ValueError, match="k and v"):
+        run(q, k, v[:15])                               # short v
+    with pytest.raises(ValueError, match="k and v"):
+        run(q, k[:, :, :32], v)                         # head_dim mismatch
+    with pytest.raises(ValueError, match=r"\[T, heads, head_dim\]"):
+        run(q, k.reshape(16, 128), v)
+    with pytest.raises(TypeError, match="dtype"):
+        run(q, k.half(), v)                             # mixed dtypes
+    with pytest.raises(TypeError, match="dtype"):
+        run(*(t.float() for t in (q, k, v)))            # fp32
+    with pytest.raises(TypeError, match="int32"):
+        run(q, k, v, cu_q=cu.long())                    # int64 metadata
+    with pytest.raises(TypeError, match="seq_is_causal"):
+        run(q, k, v, flags=torch.zeros(1, dtype=torch.float32))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        run(q, k, v)                                    # valid shapes, but no CPU path
+
+
+def test_noalloc_status_rejects_null(lib):
+    assert lib.thd_attn_noalloc_status(None, None) == vlp.THD_ERR_ARG

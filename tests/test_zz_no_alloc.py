@@ -53,3 +53,34 @@ def test_noalloc_matches_workspace_entry_point(lib, name):
         ldiff = torch.where(both_inf, torch.zeros_like(lse), (lse - ref_lse).abs()).max().item()
         assert ldiff <= LSE_ATOL, (call, ldiff)
         assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+
+
+@pytest.mark.parametrize("with_lse", [True, False])
+@pytest.mark.parametrize("name", ["padded_gaps", "tiny_mixed"])
+def test_noalloc_python_wrapper(lib, name, with_lse):
+    """The public wrapper (argument checks, marshalling, the current stream) with outputs the
+    caller allocated beforehand, with and without lse, twice in a row; the buffer's status
+    word, read through thd_attn_noalloc_status, stays clear."""
+    w = workloads.make(name)
+    dev = to_device(w)
+    ref_out, ref_lse = vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"],
+                                        dev["padded"], dev["causal"], w.batch_size, w.max_seqlen,
+                                        w.softmax_scale)
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((w.num_heads_q, w.total_tokens), dtype=torch.float32, device="cuda") if with_lse else None
+    for call in range(2):
+        out.fill_(float("nan"))
+        if lse is not None:
+            lse.fill_(float("nan"))
+        o, l = vlp.thd_attn_fwd_noalloc(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"],
+                                        dev["padded"], dev["causal"], w.batch_size, w.max_seqlen, w.softmax_scale,
+                                        out, lse)
+        assert o is out and l is lse
+        assert vlp.thd_attn_noalloc_status() == 0
+        diff = (out.float() - ref_out.float()).abs().max().item()
+        assert diff <= OUT_ATOL[w.dtype], (call, diff)
+        if lse is not None:
+            both_inf = torch.isneginf(lse) & torch.isneginf(ref_lse)
+            ldiff = torch.where(both_inf, torch.zeros_like(lse), (lse - ref_lse).abs()).max().item()
+            assert ldiff <= LSE_ATOL, (call, ldiff)
+        assert not torch.isnan(out).any()

@@ -14,8 +14,8 @@ import os
 
 import torch
 
-__all__ = ["thd_attn_fwd", "thd_attn_bwd", "thd_attn_fwd_noalloc", "thd_attn_merge", "thd_padding_mask",
-           "thd_padding_mask_cross", "MASK_PADDING", "MASK_PADDING_CAUSAL", "MASK_PADDING_CAUSAL_BOTTOM_RIGHT", "thd_attn_workspace_size", "thd_status_string",
+__all__ = ["thd_attn_fwd", "thd_attn_bwd", "thd_attn_fwd_noalloc", "thd_attn_noalloc_status", "thd_attn_merge", "thd_padding_mask",
+           "thd_padding_mask_cross", "MASK_PADDING", "MASK_PADDING_CAUSAL", "MASK_PADDING_CAUSAL_BOTTOM_RIGHT", "thd_attn_workspace_size", "thd_set_wait_limit_ns", "thd_status_string",
            "ThdError", "library_path", "load_library", "STATUS_WAIT_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -54,6 +54,8 @@ def load_library():
     lib.thd_attn_fwd_window.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, I, I, P, SZ, P]
     lib.thd_attn_fwd_noalloc.restype = I
     lib.thd_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, F, P, P, I, I, I, I, I, P]
+    lib.thd_attn_noalloc_status.restype = I
+    lib.thd_attn_noalloc_status.argtypes = [P, P]
     lib.thd_attn_bwd.restype = I
     lib.thd_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, F, P, P, P, I, I, I, I, I, P, SZ, P]
     lib.thd_attn_bwd_window.restype = I
@@ -69,6 +71,8 @@ def load_library():
     lib.thd_padding_mask.argtypes = [P, I, I, P, P]
     lib.thd_attn_workspace_size.restype = SZ
     lib.thd_attn_workspace_size.argtypes = []
+    lib.thd_set_wait_limit_ns.restype = ctypes.c_uint64
+    lib.thd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.thd_status_string.restype = ctypes.c_char_p
     lib.thd_status_string.argtypes = [I]
     _LIB = lib
@@ -80,6 +84,13 @@ _lib = load_library
 
 def thd_attn_workspace_size():
     return int(_lib().thd_attn_workspace_size())
+
+
+def thd_set_wait_limit_ns(ns):
+    """Time limit of one pipeline wait inside the kernels for later calls (0: the default,
+    2 s); returns the previous limit.  A short limit makes waits run out on purpose: the
+    call then sets STATUS_WAIT_TIMEOUT in its status word and its output is unspecified."""
+    return int(_lib().thd_set_wait_limit_ns(int(ns)))
 
 
 def thd_status_string(status):
@@ -113,6 +124,35 @@ def _check_metadata(batch_size, cu_q, cu_kv=None, pad_q=None, pad_kv=None, flags
             raise ValueError(f"{name} holds {t.numel()} entries, batch_size {batch_size} needs {need}")
 
 
+def _check_qkv(q, k, v):
+    """q [T, Hq, d], k / v [T, Hkv, d] with q's T and d, one dtype (bf16 or fp16).  The library
+    encodes its tensor maps from these sizes, so a k or v shorter than q would be read past
+    its end: refused here, before anything is launched.  Returns (T, Hq, Hkv, d)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [T, heads, head_dim]")
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (T, Hkv, d) or tuple(v.shape) != (T, Hkv, d):
+        raise ValueError("k and v must be [T, Hkv, head_dim] with q's T and head_dim")
+    if q.dtype not in (torch.bfloat16, torch.float16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share dtype bf16 or fp16")
+    return T, Hq, Hkv, d
+
+
+def _check_metadata_dtypes(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, seq_is_causal):
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv),
+                    ("cu_seqlens_q_padded", cu_seqlens_q_padded),
+                    ("cu_seqlens_kv_padded", cu_seqlens_kv_padded)):
+        if t is not None and (not isinstance(t, torch.Tensor) or t.dtype != torch.int32):
+            raise TypeError(f"{name} must be an int32 tensor")
+    if seq_is_causal is not None and (not isinstance(seq_is_causal, torch.Tensor)
+                                      or seq_is_causal.dtype not in (torch.bool, torch.uint8)):
+        raise TypeError("seq_is_causal must be a bool or uint8 tensor")
+
+
 def _check_out(t, name, shape, dtype, device):
     if t is not None and (tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device):
         raise ValueError(f"{name} must be a {dtype} tensor of shape {tuple(shape)} on {device}")
@@ -144,26 +184,13 @@ def thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     runs of short sequences into shared tiles (see thd_attn_fwd in include/thd_attn.h).
     Returns (out [T, Hq, d], lse [Hq, T] float32 or None).
     """
+    T, Hq, Hkv, d = _check_qkv(q, k, v)
+    _check_metadata_dtypes(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, seq_is_causal)
     for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
                     ("cu_seqlens_kv", cu_seqlens_kv), ("cu_seqlens_q_padded", cu_seqlens_q_padded),
                     ("cu_seqlens_kv_padded", cu_seqlens_kv_padded), ("seq_is_causal", seq_is_causal),
                     ("out", out), ("lse", lse), ("workspace", workspace)):
         _cuda(t, name)
-    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
-        raise ValueError("q, k, v must be [T, heads, head_dim]")
-    T, Hq, d = q.shape
-    Hkv = k.shape[1]
-    if k.shape != (T, Hkv, d) or v.shape != (T, Hkv, d):
-        raise ValueError("k and v must be [T, Hkv, head_dim] with q's T and head_dim")
-    if q.dtype not in (torch.bfloat16, torch.float16) or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v must share dtype bf16 or fp16")
-    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv),
-                    ("cu_seqlens_q_padded", cu_seqlens_q_padded),
-                    ("cu_seqlens_kv_padded", cu_seqlens_kv_padded)):
-        if t is not None and t.dtype != torch.int32:
-            raise TypeError(f"{name} must be int32")
-    if seq_is_causal is not None and seq_is_causal.dtype not in (torch.bool, torch.uint8):
-        raise TypeError("seq_is_causal must be bool or uint8")
     if batch_size is None:
         batch_size = cu_seqlens_q.numel() - 1
     _check_metadata(batch_size, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
@@ -197,16 +224,18 @@ def thd_attn_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padd
 
     For callers that cannot allocate device memory; the caller passes every input and
     output tensor, and nothing is allocated here either.  Calls on one device must not
-    overlap on the GPU (they share the buffer).
+    overlap on the GPU (they share the buffer).  The argument checks are those of
+    thd_attn_fwd.  thd_attn_noalloc_status() reads the buffer's device status word.
     """
+    T, Hq, Hkv, d = _check_qkv(q, k, v)
+    _check_metadata_dtypes(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, seq_is_causal)
+    if out is None:
+        raise ValueError("out must be provided")
     for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
                     ("cu_seqlens_kv", cu_seqlens_kv), ("cu_seqlens_q_padded", cu_seqlens_q_padded),
                     ("cu_seqlens_kv_padded", cu_seqlens_kv_padded), ("seq_is_causal", seq_is_causal),
                     ("out", out), ("lse", lse)):
         _cuda(t, name)
-    if out is None:
-        raise ValueError("out must be provided")
-    T, Hq, d = q.shape
     _check_metadata(batch_size, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
                     seq_is_causal)
     _check_out(out, "out", q.shape, q.dtype, q.device)
@@ -216,11 +245,23 @@ def thd_attn_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padd
             _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
             _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), _ptr(seq_is_causal),
             int(batch_size), int(max_seqlen), float(softmax_scale), _ptr(out), _ptr(lse),
-            int(T), int(Hq), int(k.shape[1]), int(d), THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16,
+            int(T), int(Hq), int(Hkv), int(d), THD_BF16 if q.dtype == torch.bfloat16 else THD_FP16,
             _stream_handle(q.device))
     if st != THD_OK:
         raise ThdError(st, "thd_attn_fwd_noalloc")
     return out, lse
+
+
+def thd_attn_noalloc_status(device=None):
+    """Device status word (STATUS_* bits) of the last thd_attn_fwd_noalloc call on `device`
+    that ran before this read: waits for the work queued so far on the current stream."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    word = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        st = _lib().thd_attn_noalloc_status(ctypes.byref(word), _stream_handle(dev))
+    if st != THD_OK:
+        raise ThdError(st, "thd_attn_noalloc_status")
+    return int(word.value)
 
 
 def thd_padding_mask(cu_seqlens, batch_size, max_seqlen, mask=None):
@@ -302,14 +343,16 @@ def thd_attn_bwd(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlen
                  softmax_scale=None, dq=None, dk=None, dv=None, workspace=None, window=(-1, -1)):
     """Gradients (dq, dk, dv) of thd_attn_fwd for the same batch and window; out / lse are
     the forward's outputs.  head_dim 64 or 128."""
+    T, Hq, Hkv, d = _check_qkv(q, k, v)
+    _check_metadata_dtypes(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, seq_is_causal)
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout),
                     ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv),
                     ("cu_seqlens_q_padded", cu_seqlens_q_padded),
                     ("cu_seqlens_kv_padded", cu_seqlens_kv_padded), ("seq_is_causal", seq_is_causal),
                     ("dq", dq), ("dk", dk), ("dv", dv), ("workspace", workspace)):
         _cuda(t, name)
-    T, Hq, d = q.shape
-    Hkv = k.shape[1]
+    if out.dtype != q.dtype or dout.dtype != q.dtype:
+        raise TypeError("out and dout must have q's dtype")
     if out.shape != q.shape or dout.shape != q.shape or lse.shape != (Hq, T) or lse.dtype != torch.float32:
         raise ValueError("out / dout must match q; lse must be float32 [Hq, T]")
     if batch_size is None:

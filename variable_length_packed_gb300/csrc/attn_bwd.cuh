@@ -140,6 +140,7 @@ struct BwdSmem {
   float lse2[kTileM];                              // LSE * log2(e) of the tile's queries
   float dd[kTileM];                                // D of the tile's queries
   uint64_t bar_kv, bar_q, bar_mma;
+  uint64_t bar_drain;   // the MMAs still in flight when the CTA leaves its loop
   uint32_t tmem_base;
   uint32_t abort;
   WorkItem item;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&sm.bar_kv, 1);
     mbar_init(&sm.bar_q, 1);
     mbar_init(&sm.bar_mma, 1);
+    mbar_init(&sm.bar_drain, 1);
     fence_mbar_init();
     sm.abort = 0;
     sched_init(sm.sched);
@@ -206,17 +208,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const float sl2 = p.scale_log2;
   volatile uint32_t* abort_flag = &sm.abort;
   uint32_t ph_kv = 0, ph_q = 0, ph_mma = 0;
-  bool q_in_flight = false;   // thread 0: a Q / dO load not yet waited for
+  // thread 0: phase parity of a K/V or Q/dO load issued and not yet waited for (-1: none),
+  // so that a CTA leaving after a wait gave up lets it land first
+  int kv_par = -1, q_par = -1;
 
   // thread 0: Q and dO rows q_start + q0 .. of query head h into shared memory
   auto load_q = [&](int h, int q_row) {
+    q_par = (int)ph_q;
     mbar_arrive_expect_tx(&sm.bar_q, 2 * kTileBytes);
 #pragma unroll
     for (int pn = 0; pn < kPanels; ++pn) {
       tma_load_2d(sm.q + pn * 16384, &tm_q, &sm.bar_q, h * p.d + pn * 64, q_row);
       tma_load_2d(sm.dout + pn * 16384, &tm_do, &sm.bar_q, h * p.d + pn * 64, q_row);
     }
-    q_in_flight = true;
   };
 
   Claimer claimer{0ull, 0};   // used by warp 0
@@ -242,6 +246,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int nqt = last_q < 0 ? 0 : (int)min((long long)nqt_all, last_q / kTileM + 1);
     const bool any = s.q_len > 0 && qt_first < nqt;
     if (any && tid == 0) {
+      kv_par = (int)ph_kv;
       mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
 #pragma unroll
       for (int pn = 0; pn < kPanels; ++pn) {
@@ -276,28 +281,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncthreads();
         // ---- S^T = K Q^T, dP^T = V dO^T ----
         if (tid == 0) {
-          if (first) mbar_wait(&sm.bar_kv, ph_kv, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
-          mbar_wait(&sm.bar_q, ph_q, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
-          q_in_flight = false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            umma_ss(tS, smem_desc_join(k_K + off, hi), smem_desc_join(q_K + off, hi), idesc_s, kk > 0 ? 1u : 0u);
+          bool ready = true;
+          if (first) {
+            ready = mbar_wait(&sm.bar_kv, ph_kv, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+            if (ready) kv_par = -1;
           }
-#pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            umma_ss(tDP, smem_desc_join(v_K + off, hi), smem_desc_join(o_K + off, hi), idesc_s, kk > 0 ? 1u : 0u);
+          if (ready) {
+            ready = mbar_wait(&sm.bar_q, ph_q, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+            if (ready) q_par = -1;
           }
-          umma_commit(&sm.bar_mma);
+          if (ready) {   // after a wait gave up nothing more is issued; the waits below give up too
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              umma_ss(tS, smem_desc_join(k_K + off, hi), smem_desc_join(q_K + off, hi), idesc_s, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              umma_ss(tDP, smem_desc_join(v_K + off, hi), smem_desc_join(o_K + off, hi), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&sm.bar_mma);
+          }
           // the previous tile's dQ staging (in the dS^T and staging buffers) was read
           // while these MMAs run; the barrier below orders it before the dS^T writes
           bulk_wait_group_read0();
         }
         if (first) ph_kv ^= 1u;
         ph_q ^= 1u;
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
         ph_mma ^= 1u;
         __syncthreads();
         tc_fence_after();
@@ -368,7 +381,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncthreads();
 
         // ---- dV += P^T dO, dK += dS^T Q, dQ_tile = dS K ----
-        if (tid == 0) {
+        if (tid == 0 && !*abort_flag) {
           tc_fence_after();
           // 16 queries per step: 8 TMEM columns of P^T / dS^T, two steps per 32-column chunk
 #pragma unroll
@@ -385,7 +398,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     kk > 0 ? 1u : 0u);
           umma_commit(&sm.bar_mma);
         }
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
         ph_mma ^= 1u;
         tc_fence_after();
         first = false;
@@ -475,13 +488,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     if (stop) break;
   }
-  if (tid == 0) bulk_wait_group0();   // dQ reductions complete
-  // a Q / dO load issued ahead lands before the CTA can exit (only after an abort)
-  if (tid == 0 && q_in_flight) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(&sm.bar_q, ph_q)) {
-      if (globaltimer_ns() - t0 > 200000000ull) break;
-    }
+  if (tid == 0) {
+    bulk_wait_group0();   // dQ reductions complete
+    // after a wait gave up: loads issued and not waited for land, and the MMAs
+    // already issued complete, before TMEM is released and the CTA exits
+    if (kv_par >= 0) drain_wait(&sm.bar_kv, (uint32_t)kv_par);
+    if (q_par >= 0) drain_wait(&sm.bar_q, (uint32_t)q_par);
+    umma_commit(&sm.bar_drain);
+    drain_wait(&sm.bar_drain, 0);
   }
 
   tc_fence_before();

@@ -24,7 +24,7 @@ namespace thd {
 
 constexpr int kBlockN = 128;            // keys per KV tile
 constexpr int kTileM = 128;             // query rows per Q tile (UMMA M)
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default limit of one pipeline wait: 2 s
 constexpr uint32_t THD_WAIT_TIMEOUT_BIT = 1u;     // device status bit of a timed-out wait
 
 struct AttnParams {
@@ -40,6 +40,7 @@ struct AttnParams {
   float* lse;              // may be null
   unsigned long long* work_counter;
   uint32_t* status;
+  uint64_t wait_limit_ns;  // a pipeline wait gives up (status bit, CTA abort) after this long
   int claim;               // work items taken per atomic on the counter (>= 1)
   int win_left, win_right; // sliding window (keys before / after the diagonal), -1 = unbounded
   int B, T, Hq, Hkv, d, group;

@@ -19,6 +19,7 @@ struct SerialSmem {
   alignas(1024) uint8_t p[kTileM * kBlockN * 2];
   uint64_t bar_load;
   uint64_t bar_mma;
+  uint64_t bar_drain;   // the MMAs still in flight when the CTA leaves its loop
   uint32_t tmem_base;
   uint32_t abort;
   WorkItem item;
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(128, 1)
   if (tid == 0) {
     mbar_init(&sm.bar_load, 1);
     mbar_init(&sm.bar_mma, 1);
+    mbar_init(&sm.bar_drain, 1);
     fence_mbar_init();
     sm.abort = 0;
     sched_init(sm.sched);
@@ -89,6 +91,7 @@ __global__ void __launch_bounds__(128, 1)
   zero_pad_rows(p, 0, blockDim.x, 2);
 
   uint32_t ph_load = 0, ph_mma = 0;
+  int load_par = -1;   // thread 0 (TMA): phase parity of a load issued and not yet waited for
   volatile uint32_t* abort_flag = &sm.abort;
 
   Claimer claimer{0ull, 0};   // used by warp 0
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(128, 1)
       // ---- Q and first K/V tile ----
       if (kTMA) {
         if (tid == 0) {
+          load_par = (int)ph_load;
           mbar_arrive_expect_tx(&sm.bar_load, 3 * kTileBytes);
 #pragma unroll
           for (int pn = 0; pn < kPanels; ++pn) {
@@ -141,9 +145,8 @@ __global__ void __launch_bounds__(128, 1)
         const int kv0 = j * kBlockN;
         // ---- S = Q K^T ----
         if (tid == 0) {
-          if (kTMA) {
-            mbar_wait(&sm.bar_load, ph_load, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
-          }
+          if (kTMA && mbar_wait(&sm.bar_load, ph_load, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns))
+            load_par = -1;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(128, 1)
           umma_commit(&sm.bar_mma);
         }
         if (kTMA) ph_load ^= 1u;
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
         ph_mma ^= 1u;
         tc_fence_after();
 
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(128, 1)
           }
           umma_commit(&sm.bar_mma);
         }
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
         ph_mma ^= 1u;
         tc_fence_after();
 
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(128, 1)
           const int kvn = (j + 1) * kBlockN;
           if (kTMA) {
             if (tid == 0) {
+              load_par = (int)ph_load;
               mbar_arrive_expect_tx(&sm.bar_load, 2 * kTileBytes);
 #pragma unroll
               for (int pn = 0; pn < kPanels; ++pn) {
@@ -302,6 +306,13 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
   }
 
+  // After a wait gave up, MMAs (and, with TMA, a load) may still be in flight:
+  // they complete before TMEM is released and the CTA exits.
+  if (tid == 0) {
+    if (load_par >= 0) drain_wait(&sm.bar_load, (uint32_t)load_par);
+    umma_commit(&sm.bar_drain);
+    drain_wait(&sm.bar_drain, 0);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

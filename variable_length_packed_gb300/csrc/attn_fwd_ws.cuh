@@ -45,6 +45,12 @@
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; P_i
 // occupies the first 64 columns of S_i (two 16-bit values per column).
+//
+// Every wait is bounded (p.wait_limit_ns).  A wait that runs out sets the CTA's
+// abort flag and the status bit; every role then leaves its loop and waits, with
+// a bound of its own and ignoring the flag, for the asynchronous work it started
+// (the producer for each TMA copy it issued, the MMA thread for its committed
+// MMAs), so no copy or MMA is in flight when TMEM is released and the CTA exits.
 #pragma once
 #include "attn_common.cuh"
 
@@ -234,19 +240,11 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
 }
 
 // Wait that also gives up when the CTA aborted.
-#define WS_WAIT(bar, parity) mbar_wait((bar), (parity), abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, kWaitLimitNs)
+#define WS_WAIT(bar, parity) mbar_wait((bar), (parity), abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns)
 
 // Warp-uniform variant: every lane waits, and the warp gives up together, so the
 // warp-collective tcgen05.ld / tcgen05.st that follow stay convergent.
 #define WS_WAIT_WARP(bar, parity) (__all_sync(0xffffffffu, WS_WAIT((bar), (parity)) ? 1 : 0) != 0)
-
-// Bounded wait used only while draining (ignores the abort flag).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 200000000ull) return;
-  }
-}
 
 // Row table of packed group g (chunk-local; -1: every row absent): row r of
 // the tile is query row r of the window that starts at the group's first
@@ -348,7 +346,10 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
         for (int pn = 0; pn < kPanels; ++pn)
           tma_load_2d(sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], kvh * p.d + pn * 64, row);
         if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT(&sm.v_empty[st], reuse);
-        if (!ok) break;
+        if (!ok) {   // the K copy just issued lands before the CTA can exit
+          drain_wait(&sm.k_full[st], (kv_cnt / kWsStages) & 1);
+          break;
+        }
         mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
 #pragma unroll
         for (int pn = 0; pn < kPanels; ++pn)
@@ -359,7 +360,10 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (!ok) break;
   }
-  // copies still in flight land before the CTA can exit
+  // copies still in flight land before the CTA can exit: every Q and K/V load
+  // counted in q_cnt / kv_cnt (the last kQSlots / kWsStages of them may still be
+  // pending; earlier ones were consumed), and a K copy whose V partner was not
+  // issued was drained above
   if (lane == 0) {
     for (uint32_t c = (q_cnt > (uint32_t)kQSlots ? q_cnt - kQSlots : 0); c < q_cnt; ++c)
       drain_wait(&sm.q_full[c % kQSlots], (c / kQSlots) & 1);
@@ -568,7 +572,7 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         const uint64_t now = globaltimer_ns();
         if (idle_t0 == 0) {
           idle_t0 = now;
-        } else if (now - idle_t0 > kWaitLimitNs) {
+        } else if (now - idle_t0 > p.wait_limit_ns) {
           *abort_flag = 1u;
           atomicOr(p.status, THD_WAIT_TIMEOUT_BIT);
           ok = false;
@@ -693,7 +697,10 @@ __device__ __forceinline__ bool ws_softmax_tile(WsSmem<DP>& sm, const AttnParams
     if (half == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
       // O_t must hold the previous P V product before it is rescaled, and the
       // rescaled O must be in TMEM before this tile's first P V step
-      if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) return false;
+      if (!WS_WAIT_WARP(&sm.o_full[tile], (o_cnt + j - 1) & 1)) {
+        tmem_st_wait();   // the P stores above complete before TMEM can be released
+        return false;
+      }
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
@@ -975,15 +982,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     ws_softmax<DT, DP, kWin, kPack>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
   }
 
+  // Every role has drained its own asynchronous work: the producer its copies in
+  // flight, the MMA thread its committed MMAs, the softmax warps their TMEM stores.
   tc_fence_before();
   __syncthreads();
-  if (sm.abort != 0u && threadIdx.x == 0) {
-    // after a wait gave up, a K copy issued just before may still be in flight
-    // (the producer drains the stages it completed): let it land
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 50000ull) {
-    }
-  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

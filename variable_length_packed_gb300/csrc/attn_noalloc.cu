@@ -19,7 +19,14 @@
 // and produce wrong results; calls on one stream, or otherwise ordered, are fine.
 // The counter and status word are cleared on the caller's stream at the start of
 // every call (by the same path thd_attn_fwd uses), so the buffer needs no
-// initialisation and keeps only the last call's contents.
+// initialisation and keeps only the last call's contents.  A pipeline wait that
+// gives up sets a bit of the status word (byte 8 of the buffer);
+// thd_attn_noalloc_status copies that word to the host.
+//
+// The buffer's device address is cached per device index for the life of the
+// process: do not keep using the entry point across cudaDeviceReset (or any
+// other teardown of the device's primary context), which may place the
+// library's device code, and so the buffer, elsewhere.
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -29,6 +36,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 256;   // the stated maximum workspace
+constexpr size_t kStatusOffset = 8;            // the status word's byte offset in the workspace
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
@@ -69,4 +77,17 @@ extern "C" int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   return thd_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
                       seq_is_causal, batch_size, max_seqlen, softmax_scale, out, lse, total_tokens, num_heads_q,
                       num_heads_kv, head_dim, dtype, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" int thd_attn_noalloc_status(uint32_t* status, void* stream) {
+  if (!status) return THD_ERR_ARG;
+  void* scratch = nullptr;
+  const int st = scratch_for_current_device(&scratch);
+  if (st != THD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // ordered after the work already queued on `stream`; the host waits for the copy
+  if (cudaMemcpyAsync(status, static_cast<char*>(scratch) + kStatusOffset, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                      s) != cudaSuccess)
+    return THD_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? THD_OK : THD_ERR_CUDA;
 }

@@ -61,14 +61,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on phase `parity` of `bar`.  Gives up when *abort is set by
 // another thread, or after `limit_ns` of wall time; on a timeout it sets
 // *abort and ORs `code` into the device status word.  Returns true when the
-// phase completed.
+// phase completed.  The flag and the clock are read after the second poll and
+// then every 16 polls (each poll may suspend the thread for a short,
+// hardware-defined time).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort,
                                           uint32_t* status, uint32_t code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 15u) == 1) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1u;
@@ -76,6 +78,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         return false;
       }
     }
+  }
+}
+
+// Bounded wait used only while a CTA drains its own asynchronous work before
+// exiting (copies in flight, committed MMAs): it ignores the abort flag, since
+// that work completes by itself, and gives up after 200 ms.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;
   }
 }
 

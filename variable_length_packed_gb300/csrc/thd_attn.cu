@@ -1,6 +1,7 @@
 // thd_attn.cu — the C ABI of libthdattn.so (declared in include/thd_attn.h):
 // host-side argument validation, TMA tensor-map encoding and kernel launches.
 // Nothing here reads device memory or synchronises a stream.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -24,6 +25,10 @@ cudaError_t launch_attn_merge(const void* out_a, const float* lse_a, const void*
 namespace {
 
 constexpr size_t kWorkspaceBytes = 256;
+
+// Limit of one pipeline wait inside the kernels, for calls made from now on
+// (thd_set_wait_limit_ns; 0 restores the default).
+std::atomic<uint64_t> g_wait_limit_ns{thd::kWaitLimitNs};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -217,6 +222,7 @@ int thd_attn_bwd_window(const void* q, const void* k, const void* v, const void*
   p.lse = const_cast<float*>(lse);
   p.work_counter = static_cast<unsigned long long*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.claim = claim_for(max_seqlen, (long long)batch_size * num_heads_kv, sms);
   p.B = batch_size;
   p.T = total_tokens;
@@ -278,6 +284,10 @@ const char* thd_status_string(int status) {
 }
 
 size_t thd_attn_workspace_size(void) { return kWorkspaceBytes; }
+
+uint64_t thd_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? thd::kWaitLimitNs : ns);
+}
 
 int thd_padding_mask(const int32_t* cu_seqlens, int batch_size, int max_seqlen, uint8_t* mask, void* stream) {
   if (batch_size < 0 || max_seqlen < 0) return THD_ERR_ARG;
@@ -367,6 +377,7 @@ int thd_attn_fwd_window(const void* q, const void* k, const void* v, const int32
   p.lse = lse;
   p.work_counter = static_cast<unsigned long long*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.claim = claim_for(max_seqlen, (long long)batch_size * num_heads_q, sms);
   p.B = batch_size;
   p.T = total_tokens;
