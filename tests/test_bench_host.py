@@ -99,3 +99,46 @@ def test_recorded_traffic_follows_the_workload():
     assert small is not None and abs(full - 4 * small) < 1.0
     assert bench.recorded_traffic("attn_fwd", "many_short") is None
     assert bench.recorded_traffic("attn_fwd") == full
+
+
+def test_other_workloads_use_their_own_seed_and_gap_fill():
+    """The batches timed beside the step draw Q/K/V from their own seed (padded gaps 1,
+    mixed GQA 2, long context 3, many short 4), with the gap rows as the batch states."""
+    for name, seed in (("padded_gaps", 1), ("mixed_gqa", 2), ("long_context", 3), ("many_short", 4)):
+        assert workloads.make(name, tensors=False).seed == seed, name
+    ow, q, k, v = bench.other_inputs("padded_gaps", "cpu")
+    rq, rk, rv = workloads.device_qkv(ow, "cpu", seed=1)
+    assert torch.equal(q, rq) and torch.equal(k, rk) and torch.equal(v, rv)
+    valid = torch.zeros(ow.total_tokens, dtype=torch.bool)
+    for s, L in zip(ow.starts, ow.lengths):
+        valid[int(s):int(s) + int(L)] = True
+    assert (~valid).any() and torch.all(q[~valid] == 100.0) and torch.all(v[~valid] == 100.0)
+    assert not torch.any(q[valid] == 100.0)
+
+
+def test_library_rebuild_follows_source_contents(tmp_path, monkeypatch):
+    """build._stale() compares a hash of the sources' contents (and the flags) with the one
+    stored beside the library: a newer file time alone does not rebuild, a changed byte does."""
+    from variable_length_packed_gb300 import build as vbuild
+    csrc, inc = tmp_path / "pkg" / "csrc", tmp_path / "include"
+    csrc.mkdir(parents=True)
+    inc.mkdir()
+    (csrc / "a.cu").write_text("int a;\n")
+    (inc / "h.h").write_text("#define X 1\n")
+    lib = tmp_path / "pkg" / "lib.so"
+    monkeypatch.setattr(vbuild, "CSRC", str(csrc))
+    monkeypatch.setattr(vbuild, "ROOT", str(tmp_path))
+    monkeypatch.setattr(vbuild, "LIB", str(lib))
+    monkeypatch.setattr(vbuild, "STAMP", str(lib) + ".sha256")
+    assert vbuild._stale()                                   # no library
+    lib.write_bytes(b"\0")
+    assert vbuild._stale()                                   # no stamp
+    (tmp_path / "pkg" / "lib.so.sha256").write_text(vbuild.source_hash() + "\n")
+    assert not vbuild._stale()
+    os.utime(csrc / "a.cu", (4e9, 4e9))                      # newer time, same bytes
+    assert not vbuild._stale()
+    (inc / "h.h").write_text("#define X 2\n")                # same size, other bytes
+    assert vbuild._stale()
+    (inc / "h.h").write_text("#define X 1\n")
+    assert not vbuild._stale()
+    assert vbuild._stale(["-DTHD_EXTRA"])                    # other flags

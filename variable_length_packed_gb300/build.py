@@ -8,6 +8,7 @@ runtime's driver entry-point query).
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -18,6 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libthdattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
+# content hash of the sources and flags the library was built from, written beside it
+STAMP = LIB + ".sha256"
 
 SOURCES = ["thd_attn.cu", "padding_mask.cu", "attn_noalloc.cu", "attn_merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -32,23 +35,37 @@ def nvcc():
     return exe
 
 
-def _stale():
-    if not os.path.exists(LIB):
-        return True
-    t = os.path.getmtime(LIB)
+def source_hash(extra_flags=()):
+    """SHA-256 over every file under csrc/ and include/ (names and contents, sorted) and the
+    compiler flags: the library is rebuilt whenever any of them differs from what it was
+    built from, whatever the files' times say."""
+    h = hashlib.sha256()
     for d in (CSRC, os.path.join(ROOT, "include")):
-        for f in os.listdir(d):
-            if os.path.getmtime(os.path.join(d, f)) > t:
-                return True
-    return False
+        for f in sorted(os.listdir(d)):
+            path = os.path.join(d, f)
+            if os.path.isfile(path):
+                h.update(os.path.relpath(path, ROOT).encode() + b"\0")
+                with open(path, "rb") as fh:
+                    h.update(fh.read())
+                h.update(b"\0")
+    h.update(" ".join([*ARCH, *FLAGS, *extra_flags]).encode())
+    return h.hexdigest()
+
+
+def _stale(extra_flags=()):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+        return True
+    with open(STAMP) as f:
+        return f.read().strip() != source_hash(extra_flags)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     """Compile (if needed) and return the path of libthdattn.so."""
-    if not force and not _stale():
+    extra = list(extra_flags or [])
+    if not force and not _stale(extra):
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
-    extra = list(extra_flags or [])
+    digest = source_hash(extra)
     procs = []
     objs = []
     for src in SOURCES:
@@ -73,6 +90,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(digest + "\n")
     return LIB
 
 

@@ -61,6 +61,8 @@ class Workload:
     q: torch.Tensor = field(repr=False)   # [T, Hq, d] CPU, dtype
     k: torch.Tensor = field(repr=False)   # [T, Hkv, d]
     v: torch.Tensor = field(repr=False)   # [T, Hkv, d]
+    seed: int = 0                         # the seed Q/K/V are drawn from
+    gap_fill: float | None = None         # value of every gap row of Q/K/V (None: random like the rest)
 
 
 @dataclass
@@ -144,7 +146,7 @@ def from_lengths(name, lengths, causal, *, gaps_before=None, trailing=0, heads_q
         seq_is_causal=flags, total_tokens=int(T), num_heads_q=heads_q,
         num_heads_kv=heads_kv, head_dim=head_dim, dtype=dtype,
         softmax_scale=float(scale), max_seqlen=int(lengths.max()) if B else 0,
-        q=q, k=k, v=v)
+        q=q, k=k, v=v, seed=int(seed), gap_fill=gap_fill)
 
 
 # ---------------------------------------------------------------------------
@@ -289,15 +291,25 @@ def make(name, tensors=True):
         _MAKE_TENSORS = True
 
 
-def device_qkv(w, device, seed=0):
+def device_qkv(w, device, seed=None):
     """Q/K/V of w's shapes and dtype drawn with a seeded generator on `device`
-    (N(0,1) in fp32, then cast), for timing runs that need no host copy."""
+    (N(0,1) in fp32, then cast), for timing runs that need no host copy.  The seed is the
+    workload's own unless given; gap rows get the workload's gap_fill when it has one.
+    (A device generator draws other numbers than the CPU one, with the same distribution.)"""
+    seed = w.seed if seed is None else seed
     g = torch.Generator(device=device).manual_seed(seed)
     shape_q = (w.total_tokens, w.num_heads_q, w.head_dim)
     shape_kv = (w.total_tokens, w.num_heads_kv, w.head_dim)
     q = torch.randn(shape_q, generator=g, device=device, dtype=torch.float32).to(w.dtype)
     k = torch.randn(shape_kv, generator=g, device=device, dtype=torch.float32).to(w.dtype)
     v = torch.randn(shape_kv, generator=g, device=device, dtype=torch.float32).to(w.dtype)
+    if w.gap_fill is not None:
+        valid = torch.zeros(w.total_tokens, dtype=torch.bool)
+        for s, L in zip(w.starts, w.lengths):
+            valid[int(s):int(s) + int(L)] = True
+        pad = (~valid).to(device)
+        for t in (q, k, v):
+            t[pad] = w.gap_fill
     return q, k, v
 
 
