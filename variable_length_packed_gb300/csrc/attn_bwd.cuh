@@ -283,11 +283,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (tid == 0) {
           bool ready = true;
           if (first) {
-            ready = mbar_wait(&sm.bar_kv, ph_kv, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+            ready = mbar_wait(&sm.bar_kv, ph_kv, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask);
             if (ready) kv_par = -1;
           }
           if (ready) {
-            ready = mbar_wait(&sm.bar_q, ph_q, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+            ready = mbar_wait(&sm.bar_q, ph_q, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask);
             if (ready) q_par = -1;
           }
           if (ready) {   // after a wait gave up nothing more is issued; the waits below give up too
@@ -310,7 +312,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (first) ph_kv ^= 1u;
         ph_q ^= 1u;
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask);
         ph_mma ^= 1u;
         __syncthreads();
         tc_fence_after();
@@ -398,7 +401,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     kk > 0 ? 1u : 0u);
           umma_commit(&sm.bar_mma);
         }
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask);
         ph_mma ^= 1u;
         tc_fence_after();
         first = false;

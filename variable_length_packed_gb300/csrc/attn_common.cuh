@@ -41,6 +41,7 @@ struct AttnParams {
   unsigned long long* work_counter;
   uint32_t* status;
   uint64_t wait_limit_ns;  // a pipeline wait gives up (status bit, CTA abort) after this long
+  uint32_t wait_check_mask;  // a waiting thread reads the clock when (polls & mask) == 0
   int claim;               // work items taken per atomic on the counter (>= 1)
   int win_left, win_right; // sliding window (keys before / after the diagonal), -1 = unbounded
   int B, T, Hq, Hkv, d, group;

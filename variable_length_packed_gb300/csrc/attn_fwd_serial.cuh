@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(128, 1)
         const int kv0 = j * kBlockN;
         // ---- S = Q K^T ----
         if (tid == 0) {
-          if (kTMA && mbar_wait(&sm.bar_load, ph_load, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns))
+          if (kTMA && mbar_wait(&sm.bar_load, ph_load, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask))
             load_par = -1;
           tc_fence_after();
 #pragma unroll
@@ -157,7 +158,8 @@ __global__ void __launch_bounds__(128, 1)
           umma_commit(&sm.bar_mma);
         }
         if (kTMA) ph_load ^= 1u;
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask);
         ph_mma ^= 1u;
         tc_fence_after();
 
@@ -240,7 +242,8 @@ __global__ void __launch_bounds__(128, 1)
           }
           umma_commit(&sm.bar_mma);
         }
-        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns);
+        mbar_wait(&sm.bar_mma, ph_mma, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                    p.wait_check_mask);
         ph_mma ^= 1u;
         tc_fence_after();
 

@@ -240,7 +240,8 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
 }
 
 // Wait that also gives up when the CTA aborted.
-#define WS_WAIT(bar, parity) mbar_wait((bar), (parity), abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns)
+#define WS_WAIT(bar, parity) \
+  mbar_wait((bar), (parity), abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns, p.wait_check_mask)
 
 // Warp-uniform variant: every lane waits, and the warp gives up together, so the
 // warp-collective tcgen05.ld / tcgen05.st that follow stay convergent.
@@ -288,6 +289,12 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0;
   bool ok = true;
   Claimer claimer{0ull, 0};
+  // packed tiles: the (chunk, group) whose row table each slot's tile holds,
+  // as chunk_base * 1024 + group + 1 (group -1: a tile without rows, whose table
+  // marks every row absent), -1 while the slot has none (slot 0 tiles 0, 1, then
+  // slot 1); the query heads of a group share the table, so it is built once per
+  // slot and group
+  long long rows_of[4] = {-1, -1, -1, -1};
   for (;;) {
     const unsigned long long w = claim_item(claimer, p);
     WsUnit u = ws_decode<kWin, kPack>(sm.sched, p, w);
@@ -299,7 +306,15 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (ok) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) ws_fill_rows(sm.rows[slot][t], sm.sched, u.g[t], lane);
+        for (int t = 0; t < 2; ++t) {
+          const long long key = (long long)sm.sched.chunk_base * 1024 + (u.g[t] + 1);
+          // registers, not an indexed array: slot is 0 or 1
+          const long long held = slot ? rows_of[2 + t] : rows_of[t];
+          if (key != held) {
+            ws_fill_rows(sm.rows[slot][t], sm.sched, u.g[t], lane);
+            if (slot) rows_of[2 + t] = key; else rows_of[t] = key;
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) {

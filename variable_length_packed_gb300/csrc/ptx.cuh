@@ -61,16 +61,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on phase `parity` of `bar`.  Gives up when *abort is set by
 // another thread, or after `limit_ns` of wall time; on a timeout it sets
 // *abort and ORs `code` into the device status word.  Returns true when the
-// phase completed.  The flag and the clock are read after the second poll and
-// then every 16 polls (each poll may suspend the thread for a short,
-// hardware-defined time).
+// phase completed.  The flag and the clock are read whenever the poll count
+// has no bit of `check_mask` set: every 256 polls by default (each poll may
+// suspend the thread for a short, hardware-defined time), every poll when a
+// short limit is asked for.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort,
-                                          uint32_t* status, uint32_t code, uint64_t limit_ns) {
+                                          uint32_t* status, uint32_t code, uint64_t limit_ns, uint32_t check_mask) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 1) {
+    if ((it & check_mask) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1u;

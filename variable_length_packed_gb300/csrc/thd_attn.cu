@@ -30,6 +30,14 @@ constexpr size_t kWorkspaceBytes = 256;
 // (thd_set_wait_limit_ns; 0 restores the default).
 std::atomic<uint64_t> g_wait_limit_ns{thd::kWaitLimitNs};
 
+// A waiting thread reads the clock every 256 polls; with a limit under 1 ms
+// (only ever set to make waits run out on purpose) it reads it at every poll,
+// so that a wait the hardware completes within a few polls still runs out.
+void set_wait_fields(thd::AttnParams& p) {
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.wait_check_mask = p.wait_limit_ns < 1000000ull ? 0u : 255u;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -222,7 +230,7 @@ int thd_attn_bwd_window(const void* q, const void* k, const void* v, const void*
   p.lse = const_cast<float*>(lse);
   p.work_counter = static_cast<unsigned long long*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
-  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  set_wait_fields(p);
   p.claim = claim_for(max_seqlen, (long long)batch_size * num_heads_kv, sms);
   p.B = batch_size;
   p.T = total_tokens;
@@ -377,7 +385,7 @@ int thd_attn_fwd_window(const void* q, const void* k, const void* v, const int32
   p.lse = lse;
   p.work_counter = static_cast<unsigned long long*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 8);
-  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  set_wait_fields(p);
   p.claim = claim_for(max_seqlen, (long long)batch_size * num_heads_q, sms);
   p.B = batch_size;
   p.T = total_tokens;
