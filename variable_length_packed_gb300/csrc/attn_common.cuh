@@ -145,10 +145,10 @@ constexpr int kSchedBuckets = 1024;
 // 128-row Q window and one 128-key K/V window (built after the sort, in the
 // sort's histogram space).
 struct PackGroups {
-  uint16_t start[kSchedChunk];      // first chunk-local sequence of group g (batch order)
+  uint16_t start[kSchedChunk];      // first chunk-local sequence of group g
   uint16_t end[kSchedChunk];        // one past its last
-  uint16_t next[kSchedChunk];       // per sequence: the first one that cannot join a group it starts
-  uint16_t jump[kSchedChunk];       // next applied 2^k times (reachability doubling)
+  uint16_t next[kSchedChunk];       // per sequence: 1 if the greedy scan restarts there (a segment starts)
+  uint16_t jump[kSchedChunk];       // the segments' first sequences, in batch order
 };
 
 struct SchedSmem {
@@ -159,10 +159,7 @@ struct SchedSmem {
   uint32_t cum[kSchedChunk + 1];    // exclusive prefix of item counts, sorted order
   int4 span[kSchedChunk];           // decoded (q_start, q_len, kv_start, kv_len) per chunk-local sequence
   uint8_t code[kSchedChunk];        // mask type code per chunk-local sequence
-  union {
-    uint16_t key[kSchedChunk];      // sort key per chunk-local sequence (sort only)
-    uint16_t reach[kSchedChunk];    // kPack: sequence starts a step of the greedy grouping
-  };
+  uint16_t key[kSchedChunk];        // sort key per chunk-local sequence (sort only)
   uint16_t order[kSchedChunk];      // chunk-local sequence ids, sorted
   int chunk_base;
   int chunk_n;
@@ -238,35 +235,44 @@ __device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i, const A
 // starts at a short sequence and takes the following short sequences while their
 // rows and keys stay in order and inside 128 rows of the group's first row and
 // 128 keys of its first key; the next short sequence starts the next group.
-// The greedy scan is a chain start -> next(start) -> ...; it is walked with
-// pointer doubling (a sequence is on the chain iff it is reached from sequence 0
-// in fewer than n steps), so the warp needs log2(n) rounds instead of one step
-// per group.  When fewer than a quarter of the short sequences could take the
-// next one into their group, packing would save few tiles: the chunk keeps one
-// (sequence, head) tile per short sequence (pack_on = 0) and skips the doubling.
+// The scan restarts at every short sequence that follows a sequence that is not
+// short, or whose rows or keys begin before the previous sequence's end (no group
+// crosses such a point), so the chunk splits into independent segments that the
+// lanes walk in parallel: each lane counts the groups of its segments, a scan
+// gives every lane its first group index, and a second walk writes the groups.
+// When fewer than a quarter of the short sequences could take the next one into
+// their group, packing would save few tiles: the chunk keeps one (sequence,
+// head) tile per short sequence (pack_on = 0) and skips the walks.
 // One full warp; s.off / s.key are free (the sort is done).
 __device__ void sched_pack_groups(SchedSmem& s, int n) {
   const int lane = threadIdx.x & 31;
   PackGroups& g = s.grp;
   uint32_t joins = 0;   // short sequences whose group could take the next one
-  for (int i = lane; i < n; i += 32) {
-    const int4 a = s.span[i];
-    int nx = i + 1;
-    if (span_is_short(a)) {
-      int qe = a.x + a.y, ke = a.z + a.w;
-      while (nx < n) {
-        const int4 b = s.span[nx];
-        if (!span_is_short(b) || b.x < qe || b.z < ke || b.x + b.y > a.x + kTileM || b.z + b.w > a.z + kBlockN)
-          break;
-        qe = b.x + b.y;
-        ke = b.z + b.w;
-        ++nx;
+  int nseg = 0;         // segments; their first sequences in g.jump, in batch order
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    bool seg = false;
+    if (i < n) {
+      const int4 a = s.span[i];
+      if (span_is_short(a)) {
+        if (i + 1 < n) {
+          const int4 b = s.span[i + 1];
+          if (span_is_short(b) && b.x >= a.x + a.y && b.z >= a.z + a.w && b.x + b.y <= a.x + kTileM &&
+              b.z + b.w <= a.z + kBlockN)
+            ++joins;
+        }
+        if (i == 0) {
+          seg = true;
+        } else {
+          const int4 pr = s.span[i - 1];
+          seg = !span_is_short(pr) || a.x < pr.x + pr.y || a.z < pr.z + pr.w;
+        }
       }
+      g.next[i] = (uint16_t)(seg ? 1 : 0);   // segment-start flag
     }
-    g.next[i] = (uint16_t)nx;
-    g.jump[i] = (uint16_t)nx;
-    s.reach[i] = (uint16_t)(i == 0 ? 1 : 0);
-    joins += nx > i + 1 ? 1 : 0;
+    const uint32_t m = __ballot_sync(0xffffffffu, seg);
+    if (seg) g.jump[nseg + __popc(m & ((1u << lane) - 1u))] = (uint16_t)i;
+    nseg += __popc(m);
   }
   joins = __reduce_add_sync(0xffffffffu, joins);
   if (4u * joins < (uint32_t)s.n_short) {
@@ -278,40 +284,37 @@ __device__ void sched_pack_groups(SchedSmem& s, int n) {
     return;
   }
   __syncwarp();
-  const int rounds = n > 1 ? 32 - __clz(n - 1) : 0;   // 2^rounds >= n
-  for (int k = 0; k < rounds; ++k) {
-    // reached after m < 2^(k+1) steps: reached after m < 2^k, or 2^k steps past one
-    // (a lane may see another lane's new mark in the same round; it is on the chain too)
-    for (int i = lane; i < n; i += 32) {
-      const int j = g.jump[i];
-      if (s.reach[i] && j < n) s.reach[j] = 1;
+  // greedy walk of the lane's segments (round robin); with `out` >= 0 the groups are
+  // written from index `out` on.  Returns the number of groups.
+  auto walk = [&](int out) -> int {
+    int ng = 0;
+    for (int r = lane; r < nseg; r += 32) {
+      const int st = g.jump[r];
+      int q0 = 0, k0 = 0, qe = 0, ke = 0;
+      for (int i = st; i < n; ++i) {
+        const int4 a = s.span[i];
+        if (!span_is_short(a) || (i > st && g.next[i] != 0)) break;
+        if (i > st && a.x >= qe && a.z >= ke && a.x + a.y <= q0 + kTileM && a.z + a.w <= k0 + kBlockN) {
+          if (out >= 0) g.end[out + ng - 1] = (uint16_t)(i + 1);   // joins the open group
+        } else {
+          if (out >= 0) {
+            g.start[out + ng] = (uint16_t)i;
+            g.end[out + ng] = (uint16_t)(i + 1);
+          }
+          ++ng;
+          q0 = a.x;
+          k0 = a.z;
+        }
+        qe = a.x + a.y;
+        ke = a.z + a.w;
+      }
     }
-    __syncwarp();
-    uint16_t nj[kSchedChunk / 32];
-#pragma unroll
-    for (int t = 0; t < kSchedChunk / 32; ++t) {
-      const int i = lane + 32 * t;
-      const int j = i < n ? (int)g.jump[i] : n;
-      nj[t] = (uint16_t)(j < n ? (int)g.jump[j] : n);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int t = 0; t < kSchedChunk / 32; ++t)
-      if (lane + 32 * t < n) g.jump[lane + 32 * t] = nj[t];
-    __syncwarp();
-  }
-  int ng = 0;
-  for (int i0 = 0; i0 < n; i0 += 32) {
-    const int i = i0 + lane;
-    const bool st = i < n && s.reach[i] && span_is_short(s.span[i]);
-    const uint32_t m = __ballot_sync(0xffffffffu, st);
-    if (st) {
-      const int pos = ng + __popc(m & ((1u << lane) - 1u));
-      g.start[pos] = (uint16_t)i;
-      g.end[pos] = g.next[i];
-    }
-    ng += __popc(m);
-  }
+    return ng;
+  };
+  const int mine = walk(-1);
+  const int first = (int)warp_incl_scan((uint32_t)mine) - mine;
+  walk(first);
+  const int ng = __shfl_sync(0xffffffffu, first + mine, 31);
   if (lane == 0) {
     s.n_groups = ng;
     s.pack_on = 1;
@@ -327,14 +330,21 @@ __device__ void sched_load_chunk(SchedSmem& s, const AttnParams& p, int base) {
   const int n = min(kSchedChunk, p.B - base);
   for (int i = lane; i < kSchedBuckets; i += 32) s.off[i] = 0u;
   __syncwarp();
-  for (int i = lane; i < n; i += 32) {
-    const SeqInfo si = load_seq(p, base + i);
-    s.span[i] = make_int4(si.q_start, si.q_len, si.kv_start, si.kv_len);
-    const int raw = p.causal ? (int)p.causal[base + i] : kMaskPadding;
-    s.code[i] = (uint8_t)(raw == kMaskPadding ? kMaskPadding : (raw == kMaskCausalBottomRight ? raw : 1));
-    const uint32_t k = seq_sort_key<kPairs>(si);
-    s.key[i] = (uint16_t)k;
-    atomicAdd(&s.off[k], 1u);
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    uint32_t k = 0xFFFFFFFFu;
+    if (i < n) {
+      const SeqInfo si = load_seq(p, base + i);
+      s.span[i] = make_int4(si.q_start, si.q_len, si.kv_start, si.kv_len);
+      const int raw = p.causal ? (int)p.causal[base + i] : kMaskPadding;
+      s.code[i] = (uint8_t)(raw == kMaskPadding ? kMaskPadding : (raw == kMaskCausalBottomRight ? raw : 1));
+      k = seq_sort_key<kPairs>(si);
+      s.key[i] = (uint16_t)k;
+    }
+    // one add per distinct key of the 32 (many sequences share a key: the adds to one
+    // bucket would otherwise be serialised)
+    const uint32_t peers = __match_any_sync(0xffffffffu, k);
+    if (i < n && lane == __ffs(peers) - 1) atomicAdd(&s.off[k], (uint32_t)__popc(peers));
   }
   __syncwarp();
   if (kPairs && lane == 0) {
