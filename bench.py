@@ -464,6 +464,36 @@ def run_gpu(args, ws, rank, local):
                         "heads_kv": ow.num_heads_kv, "head_dim": ow.head_dim, "dtype": str(ow.dtype)}
         del oq, ok_, ov, oout, olse
 
+    # ---- scheduler chunk order: the same 1500 sequences with their 4 longest last / first ----
+    chunk_order = None
+    if not args.attn_only and not args.no_chunk_order:
+        cms = {}
+        for name in ("late_long", "late_long_first"):
+            ow, oq, ok_, ov = other_inputs(name, dev)
+            ocu = torch.from_numpy(ow.cu_seqlens).to(dev)
+            ocz = torch.from_numpy(ow.seq_is_causal).to(dev)
+            oout = torch.empty_like(oq)
+            olse = torch.empty((ow.num_heads_q, ow.total_tokens), dtype=torch.float32, device=dev)
+
+            def ocall():
+                vlp.thd_attn_fwd(oq, ok_, ov, ocu, ocu, None, None, ocz, ow.batch_size, ow.max_seqlen,
+                                 ow.softmax_scale, out=oout, lse=olse, workspace=wsp)
+            for _ in range(3):
+                ocall()
+            torch.cuda.synchronize()
+            o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            o0.record(stream)
+            for _ in range(10):
+                ocall()
+            o1.record(stream)
+            torch.cuda.synchronize()
+            cms[name] = o0.elapsed_time(o1) / 10
+            del oq, ok_, ov, oout, olse
+        chunk_order = {"workload": "1500 sequences (3 scheduler chunks): 1496 of U{32..256} tokens and 4 of 12288, "
+                                   "4 heads, d=128, bf16",
+                       "long_last_ms": cms["late_long"], "long_first_ms": cms["late_long_first"],
+                       "long_last_over_long_first": cms["late_long"] / cms["late_long_first"]}
+
     # ---- sliding window (local attention, +-2048 keys around the diagonal) on the same batch ----
     window = None
     if not args.attn_only and not args.no_window:
@@ -621,6 +651,7 @@ def run_gpu(args, ws, rank, local):
         "other_workloads": others,
         "backward": backward,
         "sliding_window": window,
+        "chunk_order": chunk_order,
         "merge": merge,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.result,
@@ -651,6 +682,8 @@ def main():
                     help="other packed batches whose attention launch is timed alone (after the step)")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--no-window", action="store_true", help="skip timing the sliding-window forward")
+    ap.add_argument("--no-chunk-order", action="store_true",
+                    help="skip timing the late-long-sequence batch against its long-first twin")
     ap.add_argument("--mask-only", action="store_true",
                     help="run only the padding-mask measurement and print it; for profiler captures")
     ap.add_argument("--attn-only", action="store_true",

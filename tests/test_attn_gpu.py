@@ -110,6 +110,20 @@ def test_many_short_sampled():
     compare_sampled(w, out, lse, pairs, lambda L: np.arange(L))
 
 
+def test_long_sequences_in_a_late_chunk():
+    """1500 sequences (three scheduler chunks of 512) whose four longest sit in the last chunk:
+    every CTA visits the chunks longest first, which changes the order of the work, not its
+    results.  Sampled rows of every head of the long sequences and of 40 short ones."""
+    w = workloads.make("late_long")
+    ws = workspace()
+    out, lse = run_gpu(w, workspace=ws)
+    assert status_word(ws) == 0
+    rng = np.random.default_rng(60)
+    pairs = [(b, h) for b in range(w.batch_size - 4, w.batch_size) for h in range(w.num_heads_q)]
+    pairs += [(int(b), int(rng.integers(0, w.num_heads_q))) for b in rng.choice(w.batch_size - 4, 40, replace=False)]
+    compare_sampled(w, out, lse, pairs, lambda L: boundary_rows(L, rng, extra=8))
+
+
 # --- edge cases -----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("d,dtype", [(8, torch.float16), (16, torch.bfloat16), (32, torch.float16),

@@ -140,6 +140,8 @@ __device__ __forceinline__ int kv_first_tile(const SeqInfo& s, int q0) { return 
 // ----------------------------------------------------------------------------
 constexpr int kSchedChunk = 512;
 constexpr int kSchedBuckets = 1024;
+// Batches of up to this many chunks are visited longest chunk first (below).
+constexpr int kOrderMaxChunks = 16;
 
 // Packed groups (kPack): runs of consecutive short sequences that fit one
 // 128-row Q window and one 128-key K/V window (built after the sort, in the
@@ -167,6 +169,11 @@ struct SchedSmem {
   int n_long;                       // kPairs: long sequences, at sorted positions [0, n_long)
   int n_groups;                     // kPack: packed groups of short sequences
   int pack_on;                      // kPack: this chunk's short sequences run as packed groups
+  int n_chunks;                     // chunks of the batch (-1: the visiting order is not set up yet)
+  int ordered;                      // chunks are visited in the order `corder`, else in batch order
+  int visit;                        // chunks loaded so far
+  uint32_t cmax[kOrderMaxChunks];   // longest query sequence of each chunk
+  uint16_t corder[kOrderMaxChunks]; // chunk indices, longest first
   unsigned long long item_base;
   unsigned long long item_end;
 };
@@ -435,18 +442,68 @@ __device__ __forceinline__ unsigned long long chunk_items(const SchedSmem& s, co
   return n;
 }
 
+// Chunk visiting order: the chunks of sequences (kSchedChunk consecutive ones
+// each) are taken longest chunk first, a chunk's length being its longest query
+// sequence (ties in batch order), so that long sequences in a late chunk do not
+// start last; inside a chunk the sequences are sorted as above.  Every CTA
+// computes the same order from the device metadata (cu_seqlens_q only: its
+// batch_size + 1 entries), before loading its first chunk; batches of more than
+// kOrderMaxChunks chunks keep batch order.  One full warp.
+__device__ void sched_order_chunks(SchedSmem& s, const AttnParams& p) {
+  const int lane = threadIdx.x & 31;
+  const int nch = (p.B + kSchedChunk - 1) / kSchedChunk;
+  const bool order = nch > 1 && nch <= kOrderMaxChunks;
+  if (order) {
+    // lane l reads the cu_seqlens_q entries of sequences [16 l, 16 l + 16) of a chunk
+    constexpr int kPerLane = kSchedChunk / 32;
+#pragma unroll 2
+    for (int c = 0; c < nch; ++c) {
+      const int b0 = c * kSchedChunk + lane * kPerLane;
+      const int bend = min(p.B, (c + 1) * kSchedChunk);
+      int v[kPerLane + 1];
+#pragma unroll
+      for (int u = 0; u <= kPerLane; ++u) v[u] = b0 + u <= bend ? __ldg(p.cu_q + b0 + u) : 0;
+      long long m = 0;
+#pragma unroll
+      for (int u = 0; u < kPerLane; ++u)
+        if (b0 + u < bend) m = max(m, min((long long)v[u + 1] - v[u], (long long)p.T));
+      const uint32_t cm = __reduce_max_sync(0xffffffffu, (uint32_t)m);
+      if (lane == 0) s.cmax[c] = cm;
+    }
+    __syncwarp();
+    if (lane < nch) {
+      const uint32_t mine = s.cmax[lane];
+      int rank = 0;
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t o = s.cmax[c];
+        rank += (o > mine || (o == mine && c < lane)) ? 1 : 0;
+      }
+      s.corder[rank] = (uint16_t)lane;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    s.n_chunks = nch;
+    s.ordered = order ? 1 : 0;
+    s.visit = 0;
+  }
+  __syncwarp();
+}
+
 // Loads later chunks until the one holding global item w; false when w is
 // past the last item.  One full warp.
 template <int BLOCK_M, bool kKvSide = false, bool kPairs = false, bool kPack = false>
 __device__ bool sched_seek(SchedSmem& s, const AttnParams& p, unsigned long long w) {
   while (w >= s.item_end) {
-    const int next = s.chunk_base + s.chunk_n;
-    if (next >= p.B) return false;
+    if (s.n_chunks < 0) sched_order_chunks(s, p);
+    if (s.visit >= s.n_chunks) return false;
+    const int c = s.ordered ? (int)s.corder[s.visit] : s.visit;
     const unsigned long long base_items = s.item_end;
-    sched_load_chunk<BLOCK_M, kKvSide, kPairs, kPack>(s, p, next);
+    sched_load_chunk<BLOCK_M, kKvSide, kPairs, kPack>(s, p, c * kSchedChunk);
     if ((threadIdx.x & 31) == 0) {
       s.item_base = base_items;
       s.item_end = base_items + chunk_items<kPairs, kPack>(s, p);
+      s.visit += 1;
     }
     __syncwarp();
   }
@@ -507,6 +564,9 @@ __device__ __forceinline__ void sched_init(SchedSmem& s) {
   s.n_long = 0;
   s.n_groups = 0;
   s.pack_on = 0;
+  s.n_chunks = -1;
+  s.ordered = 0;
+  s.visit = 0;
   s.item_base = 0;
   s.item_end = 0;
 }

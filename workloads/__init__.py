@@ -265,6 +265,24 @@ def many_short(seed=4):
                         head_dim=64, dtype=torch.float16, seed=seed, with_padded=True)
 
 
+def late_long(seed=6, long_first=False):
+    """1500 sequences, three scheduler chunks of 512: 1496 with lengths U{32..256} (causal ~
+    Bernoulli(0.5)) and 4 of 12288 tokens (causal, full, causal, full) placed last, in the last
+    chunk (long_first: the same sequences with the 4 long ones first); 4 heads, d=128, bf16, no
+    gaps.  The long sequences' blocks are the longest units of the launch."""
+    rng = np.random.default_rng(seed)
+    short = rng.integers(32, 257, size=1496)
+    short_causal = rng.random(1496) < 0.5
+    long_ = np.full(4, 12288)
+    long_causal = np.array([True, False, True, False])
+    if long_first:
+        lengths, causal = np.r_[long_, short], np.r_[long_causal, short_causal]
+    else:
+        lengths, causal = np.r_[short, long_], np.r_[short_causal, long_causal]
+    return from_lengths("late_long_first" if long_first else "late_long", lengths, causal, heads_q=4,
+                        head_dim=128, dtype=torch.bfloat16, seed=seed, with_padded=False)
+
+
 WORKLOADS = {
     "tiny_mixed": tiny_mixed,
     "page1": lambda: page1_constant(False),
@@ -274,6 +292,8 @@ WORKLOADS = {
     "long_context": long_context,
     "long_context_small": long_context_small,
     "many_short": many_short,
+    "late_long": late_long,
+    "late_long_first": lambda: late_long(long_first=True),
 }
 
 
