@@ -4,7 +4,7 @@
 // One CTA per SM.  A work item is two 128-row Q tiles of one sequence that share
 // every K/V tile: the same 128 rows of two query heads of one group when the
 // number of query heads per K/V head is even, else a block of 256 rows of one
-// query head:
+// query head.  Twelve warps in three warpgroups:
 //
 //   warp 0      scheduler + TMA producer: claims items from the global counter,
 //               publishes them to the other warps, loads Q (both tiles) and the
@@ -14,7 +14,8 @@
 //               then O_i += P_i V_j with P_i read from TMEM (TS UMMA); the two
 //               tiles alternate so one tile's softmax overlaps the other
 //               tile's MMAs.
-//   warps 2-5   softmax of Q tile 0; warps 6-9 softmax of Q tile 1.  One thread
+//   warps 2-3   write the pad rows' zeros, then wait at the end.
+//   warps 4-7   softmax of Q tile 0; warps 8-11 softmax of Q tile 1.  One thread
 //               per query row (= TMEM lane): masking, online max / sum, P
 //               (rounded to the input type) written over S in TMEM in two
 //               halves of 64 keys (the MMA warp starts P V on the first half
@@ -61,7 +62,13 @@ constexpr int kWsBlockM = 256;   // query rows per work item (two Q tiles)
 // two K/V stages; head_dim 64 has room for two Q slots (the next item's Q loads
 // while the current one computes) and four K/V stages.
 template <int DP> struct WsDepth { static constexpr int kQSlots = DP == 64 ? 2 : 1, kStages = DP == 64 ? 4 : 2; };
-constexpr int kWsThreads = 320;  // 10 warps
+constexpr int kWsThreads = 384;  // 12 warps: three warpgroups
+// Registers per thread after the split (setmaxnreg): the first warpgroup
+// (producer, MMA issuer, pad-row warps) gives registers to the two softmax
+// warpgroups, whose rows of S take most of them; the split adds up to what the
+// block is launched with (384 threads x 168 registers).
+constexpr uint32_t kRegsCtl = 112, kRegsSoftmax = 192;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= 384 * 168, "register split within the launch's registers");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 // One 128-row Q tile of a work unit.
@@ -839,7 +846,7 @@ __device__ __forceinline__ bool ws_packed_tile(WsSmem<DP>& sm, const AttnParams&
 }
 
 // ---------------------------------------------------------------------------
-// warps 2-9: softmax + epilogue, tile = (warp - 2) / 4
+// warps 4-11: softmax + epilogue, tile = warp / 4 - 1
 // ---------------------------------------------------------------------------
 template <typename DT, int DP, bool kWin, bool kPack>
 __device__ void ws_softmax(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, int tile,
@@ -987,14 +994,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort;
 
-  if (warp == 0) {
-    ws_producer<DP, kWin, kPack>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
-  } else if (warp == 1) {
-    if (lane == 0) ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
-    __syncwarp();
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == 0) {
+      ws_producer<DP, kWin, kPack>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
+    } else if (warp == 1) {
+      if (lane == 0) ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
+      __syncwarp();
+    } else {
+      zero_pad_rows(p, 64, 64, 2);
+    }
   } else {
-    zero_pad_rows(p, 64, kWsThreads - 64, 2);
-    ws_softmax<DT, DP, kWin, kPack>(sm, p, tmem, (warp - 2) >> 2, abort_flag);
+    setmaxnreg_inc<kRegsSoftmax>();
+    ws_softmax<DT, DP, kWin, kPack>(sm, p, tmem, (warp >> 2) - 1, abort_flag);
   }
 
   // Every role has drained its own asynchronous work: the producer its copies in
