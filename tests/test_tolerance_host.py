@@ -85,3 +85,83 @@ def test_whole_sample_count_passes_correctly_rounded_pieces():
         ref = rng.normal(0.0, 1.0, size=(37, 128))
         acc.add(torch.from_numpy(ref).to(torch.bfloat16).double().numpy(), ref)
     assert acc.check() < 0.0157
+
+
+# --- the backward's per-element gradient bound -------------------------------------------
+
+def _emulated_backward(w, dout, drop_d=False, slip=0.0):
+    """A backward that rounds exactly where the GPU's does (forward output O, P before the
+    P^T dO product, dS before the dS Q / dS K products, and each gradient), in fp64 otherwise.
+    ``drop_d`` and ``slip`` plant mistakes: dS without the D term, a relative error on dK."""
+    import oracle
+    dt = w.dtype
+    rnd = lambda x: torch.from_numpy(x).to(dt).double().numpy()
+    q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
+    do = dout.double().numpy()
+    Hq, group, sc = q.shape[1], q.shape[1] // k.shape[1], w.softmax_scale
+    dq, dk, dv, out = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(q)
+    starts, lens = oracle.sequence_spans(w.cu_seqlens, w.cu_seqlens_padded, w.batch_size)
+    for b in range(w.batch_size):
+        L, s = int(lens[b]), slice(int(starts[b]), int(starts[b]) + int(lens[b]))
+        if L <= 0:
+            continue
+        r = np.array([oracle.visible_range(i, L, L, int(w.seq_is_causal[b])) for i in range(L)])
+        vis = (np.arange(L)[None] >= r[:, :1]) & (np.arange(L)[None] < r[:, 1:])
+        for h in range(Hq):
+            g = h // group
+            Q, K, V, dO = q[s, h], k[s, g], v[s, g], do[s, h]
+            Z = np.where(vis, sc * Q @ K.T, -np.inf)
+            E = np.where(vis, np.exp(Z - Z.max(axis=1)[:, None]), 0.0)
+            P = E / E.sum(axis=1)[:, None]
+            O = rnd(P @ V)
+            out[s, h] = O
+            D = 0.0 if drop_d else (dO * O).sum(axis=1)[:, None]
+            dS = rnd(P * (dO @ V.T - D))
+            dv[s, g] += rnd(P).T @ dO
+            dk[s, g] += sc * (dS.T @ Q) * (1.0 + slip)
+            dq[s, h] += sc * dS @ K
+    return [rnd(x) for x in (dq, dk, dv)], torch.from_numpy(out).to(dt)
+
+
+def _largest_share(w, got, out, dout):
+    import oracle
+    from thd_testutil import UNIT, gradient_bounds
+    meta = (w.cu_seqlens, w.cu_seqlens, w.cu_seqlens_padded, w.cu_seqlens_padded, w.seq_is_causal, w.batch_size)
+    ref = oracle.thd_attention_bwd(w.q, w.k, w.v, dout, *meta, w.softmax_scale)
+    bounds = gradient_bounds(w, dout, out, *meta)
+    shares = []
+    for g, r, b in zip(got, ref, bounds):
+        bound = b + 2 * UNIT[w.dtype] * np.abs(r) + 1e-6 * np.abs(r).max()
+        shares.append(float((np.abs(g - r) / bound).max()))
+    return shares
+
+
+@pytest.fixture(scope="module", params=[torch.bfloat16, torch.float16])
+def small_backward(request):
+    import workloads
+    w = workloads.from_lengths("bound", [1, 37, 130, 64], [1, 0, 1, 0], gaps_before=[2, 0, 5, 1], trailing=3,
+                               heads_q=4, heads_kv=2, head_dim=64, dtype=request.param, seed=21)
+    return w, workloads.grad_output(w, 5)
+
+
+def test_gradient_bound_holds_for_the_rounding_it_models(small_backward):
+    w, dout = small_backward
+    got, out = _emulated_backward(w, dout)
+    assert max(_largest_share(w, got, out, dout)) < 0.9
+
+
+def test_gradient_bound_catches_a_dropped_d_term(small_backward):
+    w, dout = small_backward
+    got, out = _emulated_backward(w, dout, drop_d=True)
+    dq, dk, dv = _largest_share(w, got, out, dout)
+    assert dq > 1.0 and dk > 1.0 and dv < 1.0
+
+
+def test_gradient_bound_catches_a_slip_of_eight_roundoffs(small_backward):
+    """dK off by 8 u relative (3.1 % in bf16, 0.4 % in fp16) fails: the bound is a few u of the
+    terms' magnitude, not a fraction of the tensor's largest value."""
+    from thd_testutil import UNIT
+    w, dout = small_backward
+    got, out = _emulated_backward(w, dout, slip=8 * UNIT[w.dtype])
+    dq, dk, dv = _largest_share(w, got, out, dout)
+    assert dk > 1.0 and dq < 1.0 and dv < 1.0

@@ -149,3 +149,66 @@ def compare_sampled(w, out, lse, pairs, rows_for):
 def boundary_rows(L, rng, extra=6):
     base = [0, 1, 2, 63, 64, 127, 128, 129, 255, 256, L // 2, L - 2, L - 1]
     return base + list(rng.integers(0, L, size=extra))
+
+
+# Unit roundoff of the input types (the backward rounds P and dS to these).
+UNIT = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
+
+
+def gradient_bounds(w, dout, out_gpu, cu_q, cu_kv, pad_q, pad_kv, codes, batch):
+    """Per-element error bounds (dq, dk, dv) of a backward that rounds once to the input type
+    where its MMAs take a computed operand.  No bound is stated for gradients ("Add
+    per-sequence causal policy to packed THD attention", Validation, asks for parity only);
+    this one follows from the steps of the chain rule the backward takes.
+
+    Every gradient element is a sum of terms in which one factor was rounded once:
+        dV_j = sum_i P_ij dO_i            P rounded (the P^T dO MMA)
+        dK_j = scale sum_i dS_ij Q_i      dS rounded
+        dQ_i = scale sum_j dS_ij K_j      dS rounded
+    With u the unit roundoff (2^-8 bf16, 2^-11 fp16) each term is off by at most u of its
+    own magnitude, so a sum is off by at most u M, M the sum of the terms' absolute values.
+    One more difference is known exactly: D = rowsum(dO * O) is formed from the rounded
+    forward output out_gpu, not the exact one, so dS moves by P * (D_gpu - D); its effect
+    on dK and dQ is T.  Returned: 2 u M + 1.5 T per element (the factors cover the fp32
+    products, sums and exponentials, each far below u); the caller adds 2 u |ref| for the
+    output's own rounding.  dK / dV sum the group's query heads."""
+    q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
+    do = dout.double().numpy()
+    og = out_gpu.float().cpu().double().numpy()
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    group = Hq // Hkv
+    scale = w.softmax_scale
+    u = UNIT[w.dtype]
+    mq, tq = np.zeros_like(q), np.zeros_like(q)
+    mk, tk = np.zeros_like(k), np.zeros_like(k)
+    mv = np.zeros_like(v)
+    qs, ql = oracle.sequence_spans(cu_q, pad_q, batch)
+    ks, kl = oracle.sequence_spans(cu_kv, pad_kv, batch)
+    for b in range(batch):
+        Lq, Lkv = int(ql[b]), int(kl[b])
+        if Lq <= 0 or Lkv <= 0:
+            continue
+        code = 0 if codes is None else int(codes[b])
+        ranges = np.array([oracle.visible_range(i, Lq, Lkv, code) for i in range(Lq)])
+        keys = np.arange(Lkv)[None, :]
+        visible = (keys >= ranges[:, :1]) & (keys < ranges[:, 1:])
+        sq, sk = slice(qs[b], qs[b] + Lq), slice(ks[b], ks[b] + Lkv)
+        for h in range(Hq):
+            g = h // group
+            Q, K, V, dO, Og = q[sq, h], k[sk, g], v[sk, g], do[sq, h], og[sq, h]
+            Z = np.where(visible, scale * (Q @ K.T), -np.inf)
+            zmax = np.where(visible.any(axis=1), Z.max(axis=1), 0.0)
+            E = np.where(visible, np.exp(Z - zmax[:, None]), 0.0)
+            den = E.sum(axis=1)
+            P = E / np.where(den > 0, den, 1.0)[:, None]
+            dP = dO @ V.T
+            D = (dO * (P @ V)).sum(axis=1)
+            dD = np.abs((dO * Og).sum(axis=1) - D)
+            dS = P * (dP - D[:, None])
+            mv[sk, g] += np.abs(P).T @ np.abs(dO)
+            mk[sk, g] += scale * (np.abs(dS).T @ np.abs(Q))
+            tk[sk, g] += scale * ((P * dD[:, None]).T @ np.abs(Q))
+            mq[sq, h] += scale * (np.abs(dS) @ np.abs(K))
+            tq[sq, h] += scale * dD[:, None] * (P @ np.abs(K))
+    return 2 * u * mq + 1.5 * tq, 2 * u * mk + 1.5 * tk, 2 * u * mv
