@@ -149,8 +149,10 @@ constexpr int kOrderMaxChunks = 16;
 struct PackGroups {
   uint16_t start[kSchedChunk];      // first chunk-local sequence of group g
   uint16_t end[kSchedChunk];        // one past its last
-  uint16_t next[kSchedChunk];       // per sequence: 1 if the greedy scan restarts there (a segment starts)
   uint16_t jump[kSchedChunk];       // the segments' first sequences, in batch order
+  uint32_t seg[kSchedChunk / 32];   // bit i: the greedy scan restarts at sequence i (a segment starts)
+  uint32_t member[kSchedChunk / 32];  // bit i: sequence i is short (it belongs to a group)
+  uint32_t first[kSchedChunk / 32];   // bit i: sequence i starts a group
 };
 
 struct SchedSmem {
@@ -244,42 +246,53 @@ __device__ __forceinline__ SeqInfo cached_seq(const SchedSmem& s, int i, const A
 // 128 keys of its first key; the next short sequence starts the next group.
 // The scan restarts at every short sequence that follows a sequence that is not
 // short, or whose rows or keys begin before the previous sequence's end (no group
-// crosses such a point), so the chunk splits into independent segments that the
-// lanes walk in parallel: each lane counts the groups of its segments, a scan
-// gives every lane its first group index, and a second walk writes the groups.
-// When fewer than a quarter of the short sequences could take the next one into
-// their group, packing would save few tiles: the chunk keeps one (sequence,
-// head) tile per short sequence (pack_on = 0) and skips the walks.
-// One full warp; s.off / s.key are free (the sort is done).
+// crosses such a point), so the chunk splits into independent segments.  The
+// lanes walk their segments (round robin) in one flat loop and mark each group's
+// first sequence in a bitmask; a group then ends at the next marked sequence or
+// at the next sequence that is not short, and the groups are numbered in batch
+// order by counting marks.  When fewer than a quarter of the short sequences
+// could take the next one into their group, packing would save few tiles: the
+// chunk keeps one (sequence, head) tile per short sequence (pack_on = 0) and
+// skips the walk.  One full warp; s.off / s.key are free (the sort is done).
 __device__ void sched_pack_groups(SchedSmem& s, int n) {
   const int lane = threadIdx.x & 31;
   PackGroups& g = s.grp;
+  const int nwords = (n + 31) >> 5;
   uint32_t joins = 0;   // short sequences whose group could take the next one
   int nseg = 0;         // segments; their first sequences in g.jump, in batch order
+  int4 prev = make_int4(0, 0, 0, 0);   // the sequence before this lane's (lane 31's: the next batch's lane 0)
+  bool prev_short = false;
   for (int i0 = 0; i0 < n; i0 += 32) {
     const int i = i0 + lane;
-    bool seg = false;
-    if (i < n) {
-      const int4 a = s.span[i];
-      if (span_is_short(a)) {
-        if (i + 1 < n) {
-          const int4 b = s.span[i + 1];
-          if (span_is_short(b) && b.x >= a.x + a.y && b.z >= a.z + a.w && b.x + b.y <= a.x + kTileM &&
-              b.z + b.w <= a.z + kBlockN)
-            ++joins;
-        }
-        if (i == 0) {
-          seg = true;
-        } else {
-          const int4 pr = s.span[i - 1];
-          seg = !span_is_short(pr) || a.x < pr.x + pr.y || a.z < pr.z + pr.w;
-        }
-      }
-      g.next[i] = (uint16_t)(seg ? 1 : 0);   // segment-start flag
+    const int4 a = i < n ? s.span[i] : make_int4(0, 0, 0, 0);
+    const bool sh = i < n && span_is_short(a);
+    int4 pr;
+    pr.x = __shfl_up_sync(0xffffffffu, a.x, 1);
+    pr.y = __shfl_up_sync(0xffffffffu, a.y, 1);
+    pr.z = __shfl_up_sync(0xffffffffu, a.z, 1);
+    pr.w = __shfl_up_sync(0xffffffffu, a.w, 1);
+    bool pr_sh = __shfl_up_sync(0xffffffffu, sh ? 1 : 0, 1) != 0;
+    if (lane == 0) {
+      pr = prev;
+      pr_sh = prev_short;
     }
-    const uint32_t m = __ballot_sync(0xffffffffu, seg);
-    if (seg) g.jump[nseg + __popc(m & ((1u << lane) - 1u))] = (uint16_t)i;
-    nseg += __popc(m);
+    const bool ordered = a.x >= pr.x + pr.y && a.z >= pr.z + pr.w;
+    const bool seg = sh && (i == 0 || !pr_sh || !ordered);
+    if (sh && i > 0 && pr_sh && ordered && a.x + a.y <= pr.x + kTileM && a.z + a.w <= pr.z + kBlockN) ++joins;
+    const uint32_t m_seg = __ballot_sync(0xffffffffu, seg);
+    const uint32_t m_sh = __ballot_sync(0xffffffffu, sh);
+    if (lane == 0) {
+      g.seg[i0 >> 5] = m_seg;
+      g.member[i0 >> 5] = m_sh;
+      g.first[i0 >> 5] = 0u;
+    }
+    if (seg) g.jump[nseg + __popc(m_seg & ((1u << lane) - 1u))] = (uint16_t)i;
+    nseg += __popc(m_seg);
+    prev.x = __shfl_sync(0xffffffffu, a.x, 31);
+    prev.y = __shfl_sync(0xffffffffu, a.y, 31);
+    prev.z = __shfl_sync(0xffffffffu, a.z, 31);
+    prev.w = __shfl_sync(0xffffffffu, a.w, 31);
+    prev_short = __shfl_sync(0xffffffffu, sh ? 1 : 0, 31) != 0;
   }
   joins = __reduce_add_sync(0xffffffffu, joins);
   if (4u * joins < (uint32_t)s.n_short) {
@@ -291,37 +304,50 @@ __device__ void sched_pack_groups(SchedSmem& s, int n) {
     return;
   }
   __syncwarp();
-  // greedy walk of the lane's segments (round robin); with `out` >= 0 the groups are
-  // written from index `out` on.  Returns the number of groups.
-  auto walk = [&](int out) -> int {
-    int ng = 0;
-    for (int r = lane; r < nseg; r += 32) {
-      const int st = g.jump[r];
-      int q0 = 0, k0 = 0, qe = 0, ke = 0;
-      for (int i = st; i < n; ++i) {
-        const int4 a = s.span[i];
-        if (!span_is_short(a) || (i > st && g.next[i] != 0)) break;
-        if (i > st && a.x >= qe && a.z >= ke && a.x + a.y <= q0 + kTileM && a.z + a.w <= k0 + kBlockN) {
-          if (out >= 0) g.end[out + ng - 1] = (uint16_t)(i + 1);   // joins the open group
-        } else {
-          if (out >= 0) {
-            g.start[out + ng] = (uint16_t)i;
-            g.end[out + ng] = (uint16_t)(i + 1);
-          }
-          ++ng;
-          q0 = a.x;
-          k0 = a.z;
-        }
-        qe = a.x + a.y;
-        ke = a.z + a.w;
+  // greedy walk of the lane's segments, one sequence per step
+  {
+    int r = lane;
+    int st = r < nseg ? (int)g.jump[r] : 0, i = st;
+    int q0 = 0, k0 = 0, qe = 0, ke = 0;
+    while (r < nseg) {
+      const bool in_seg = i < n && ((g.member[i >> 5] >> (i & 31)) & 1u) != 0 &&
+                          (i == st || ((g.seg[i >> 5] >> (i & 31)) & 1u) == 0);
+      if (!in_seg) {   // next segment of this lane
+        r += 32;
+        if (r < nseg) st = i = (int)g.jump[r];
+        continue;
       }
+      const int4 a = s.span[i];
+      if (i == st || a.x < qe || a.z < ke || a.x + a.y > q0 + kTileM || a.z + a.w > k0 + kBlockN) {
+        atomicOr(&g.first[i >> 5], 1u << (i & 31));   // starts a group
+        q0 = a.x;
+        k0 = a.z;
+      }
+      qe = a.x + a.y;
+      ke = a.z + a.w;
+      ++i;
     }
-    return ng;
-  };
-  const int mine = walk(-1);
-  const int first = (int)warp_incl_scan((uint32_t)mine) - mine;
-  walk(first);
-  const int ng = __shfl_sync(0xffffffffu, first + mine, 31);
+  }
+  __syncwarp();
+  // groups in batch order: lane w numbers the group starts in word w, and a group
+  // ends at the next start or at the next sequence that is not short
+  const uint32_t fw = lane < nwords ? g.first[lane] : 0u;
+  const int cnt = __popc(fw);
+  const int base = (int)warp_incl_scan((uint32_t)cnt) - cnt;
+  uint32_t rest = fw;
+  for (int k = 0; rest != 0u; ++k) {
+    const int bit = __ffs(rest) - 1;
+    rest &= rest - 1u;
+    const int pos = 32 * lane + bit;
+    // stops after pos: later starts and sequences that are not short (none past n)
+    uint32_t stops = (fw | ~g.member[lane]) & ~((2u << bit) - 1u);
+    int w = lane;
+    while (stops == 0u && ++w < nwords) stops = g.first[w] | ~g.member[w];
+    const int end = stops != 0u ? min(32 * w + __ffs(stops) - 1, n) : n;
+    g.start[base + k] = (uint16_t)pos;
+    g.end[base + k] = (uint16_t)end;
+  }
+  const int ng = __shfl_sync(0xffffffffu, base + cnt, 31);
   if (lane == 0) {
     s.n_groups = ng;
     s.pack_on = 1;
