@@ -225,24 +225,24 @@ __device__ __forceinline__ WsUnit ws_decode(SchedSmem& s, const AttnParams& p, u
 // 128-byte swizzle row; the second 64-column panel starts 16 KB further).
 // q_lo / k_lo are the low descriptor words of the tiles' first K step.
 template <int DP>
-__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_lo, uint32_t idesc) {
+__device__ __forceinline__ void issue_qk(bool leader, uint32_t tS, uint32_t q_lo, uint32_t k_lo, uint32_t idesc) {
   constexpr uint32_t hi = smem_desc_sw128_hi(1024);
 #pragma unroll
   for (int kk = 0; kk < DP / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-    umma_ss(tS, smem_desc_join(q_lo + off, hi), smem_desc_join(k_lo + off, hi), idesc, kk > 0 ? 1u : 0u);
+    umma_ss_if(leader, tS, smem_desc_join(q_lo + off, hi), smem_desc_join(k_lo + off, hi), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // O += P[:, 16*k0 : 16*k1] V[16*k0 : 16*k1, :].  v_lo is the low descriptor word
 // of the V tile (MN-major: the next 64 head-dim columns are 16 KB further).
 template <int k0, int k1>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, uint32_t idesc, bool acc) {
+__device__ __forceinline__ void issue_pv(bool leader, uint32_t tO, uint32_t tP, uint32_t v_lo, uint32_t idesc, bool acc) {
   constexpr uint32_t hi = smem_desc_sw128_hi(1024);
 #pragma unroll
   for (int kk = k0; kk < k1; ++kk) {
     // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2048 bytes) of V
-    umma_ts(tO, tP + kk * 8, smem_desc_join(v_lo + kk * (2048 >> 4), hi), idesc, (acc || kk > 0) ? 1u : 0u);
+    umma_ts_if(leader, tO, tP + kk * 8, smem_desc_join(v_lo + kk * (2048 >> 4), hi), idesc, (acc || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -253,6 +253,12 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
 // Warp-uniform variant: every lane waits, and the warp gives up together, so the
 // warp-collective tcgen05.ld / tcgen05.st that follow stay convergent.
 #define WS_WAIT_WARP(bar, parity) (__all_sync(0xffffffffu, WS_WAIT((bar), (parity)) ? 1 : 0) != 0)
+
+// Non-blocking phase test with lane 0's answer for the whole warp (the MMA warp
+// polls several barriers and must take every decision together).
+__device__ __forceinline__ bool warp_test_wait(uint64_t* bar, uint32_t parity) {
+  return __shfl_sync(0xffffffffu, mbar_test_wait(bar, parity) ? 1 : 0, 0) != 0;
+}
 
 // Row table of packed group g (chunk-local; -1: every row absent): row r of
 // the tile is query row r of the window that starts at the group's first
@@ -414,10 +420,12 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   const uint32_t k_lo0 = smem_desc_sw128_lo(smem_u32(sm.k[0]), 16);
   const uint32_t v_lo0 = smem_desc_sw128_lo(smem_u32(sm.v[0]), 16384);
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0, p_cnt[2] = {0, 0};
+  // the lane that issues every MMA and commit (a commit tracks its own thread's MMAs)
+  const bool leader = elect_one_sync();
 
   auto fetch = [&](MmaUnit& x) -> bool {
     const int slot = it_cnt & 1;
-    if (!WS_WAIT(&sm.item_full[slot], (it_cnt >> 1) & 1)) return false;
+    if (!WS_WAIT_WARP(&sm.item_full[slot], (it_cnt >> 1) & 1)) return false;
     const WsUnit& w = sm.items[slot];
     x.valid = w.valid;
     x.paired = w.paired;
@@ -428,7 +436,8 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
       x.j0[t] = kWin ? w.t[t].j0 : 0;
       x.n[t] = w.t[t].n;
     }
-    mbar_arrive(&sm.item_empty[slot]);
+    __syncwarp();   // every lane has read the unit before the slot is released
+    if (leader) mbar_arrive(&sm.item_empty[slot]);
     ++it_cnt;
     return true;
   };
@@ -437,11 +446,11 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
   auto pair_s = [&](const MmaUnit& x, int t, uint32_t q_lo0, uint32_t kv_base) -> bool {
     const uint32_t c = kv_base + ((t == 1 && x.n[0] > 0) ? 1u : 0u);
     const int st = c % kWsStages;
-    if (!WS_WAIT(&sm.k_full[st], (c / kWsStages) & 1)) return false;
+    if (!WS_WAIT_WARP(&sm.k_full[st], (c / kWsStages) & 1)) return false;
     tc_fence_after();
-    issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + st * kStep, idesc_qk);
-    umma_commit(&sm.s_full[t]);
-    umma_commit(&sm.k_empty[st]);
+    issue_qk<DP>(leader, tS[t], q_lo0 + t * kStep, k_lo0 + st * kStep, idesc_qk);
+    umma_commit_if(leader, &sm.s_full[t]);
+    umma_commit_if(leader, &sm.k_empty[st]);
     return true;
   };
 
@@ -459,53 +468,53 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
       // KV tiles jb .. jb + n - 1 are ring positions kv_cnt ..; tile t visits [j0_t, n_t).
       const int n = u.n_all, jb = u.jb;
       const int qs = q_cnt % kQSlots;
-      if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
+      if (!WS_WAIT_WARP(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
       ++q_cnt;
       const uint32_t q_lo0 = q_lo00 + qs * 2 * kStep;   // this slot's tile 0
-      if (!WS_WAIT(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
+      if (!WS_WAIT_WARP(&sm.k_full[kv_cnt % kWsStages], (kv_cnt / kWsStages) & 1)) break;
       tc_fence_after();
       {
         const uint32_t ks = k_lo0 + (kv_cnt % kWsStages) * kStep;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (u.n[t] > 0 && u.j0[t] == jb) {
-            issue_qk<DP>(tS[t], q_lo0 + t * kStep, ks, idesc_qk);
-            umma_commit(&sm.s_full[t]);
+            issue_qk<DP>(leader, tS[t], q_lo0 + t * kStep, ks, idesc_qk);
+            umma_commit_if(leader, &sm.s_full[t]);
           }
         }
-        umma_commit(&sm.k_empty[kv_cnt % kWsStages]);
-        if (n == 1) umma_commit(&sm.q_empty[qs]);
+        umma_commit_if(leader, &sm.k_empty[kv_cnt % kWsStages]);
+        if (n == 1) umma_commit_if(leader, &sm.q_empty[qs]);
       }
       bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
         const int j = jb + i;
         const uint32_t c = kv_cnt + i, cn = c + 1;
         const int st = c % kWsStages, stn = cn % kWsStages;
-        if (!WS_WAIT(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
+        if (!WS_WAIT_WARP(&sm.v_full[st], (c / kWsStages) & 1)) { ok = false; break; }
         const uint32_t vs = v_lo0 + st * kStep;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (j >= u.j0[t] && j < u.n[t]) {
             const uint32_t par = p_cnt[t] & 1;
             ++p_cnt[t];
-            if (!WS_WAIT(&sm.p_lo[t], par)) { ok = false; break; }
+            if (!WS_WAIT_WARP(&sm.p_lo[t], par)) { ok = false; break; }
             tc_fence_after();
-            issue_pv<0, 4>(tO[t], tS[t], vs, idesc_pv, j > u.j0[t]);
-            if (!WS_WAIT(&sm.p_hi[t], par)) { ok = false; break; }
+            issue_pv<0, 4>(leader, tO[t], tS[t], vs, idesc_pv, j > u.j0[t]);
+            if (!WS_WAIT_WARP(&sm.p_hi[t], par)) { ok = false; break; }
             tc_fence_after();
-            issue_pv<4, 8>(tO[t], tS[t], vs, idesc_pv, true);
-            umma_commit(&sm.o_full[t]);
+            issue_pv<4, 8>(leader, tO[t], tS[t], vs, idesc_pv, true);
+            umma_commit_if(leader, &sm.o_full[t]);
           }
           if (j + 1 >= u.j0[t] && j + 1 < u.n[t]) {   // the tile's next S (or its first)
-            if (!WS_WAIT(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
+            if (!WS_WAIT_WARP(&sm.k_full[stn], (cn / kWsStages) & 1)) { ok = false; break; }
             tc_fence_after();
-            issue_qk<DP>(tS[t], q_lo0 + t * kStep, k_lo0 + stn * kStep, idesc_qk);
-            umma_commit(&sm.s_full[t]);
+            issue_qk<DP>(leader, tS[t], q_lo0 + t * kStep, k_lo0 + stn * kStep, idesc_qk);
+            umma_commit_if(leader, &sm.s_full[t]);
           }
         }
-        if (i + 1 < n) umma_commit(&sm.k_empty[stn]);   // every S MMA on K stage stn issued
-        if (i == n - 2) umma_commit(&sm.q_empty[qs]);    // last S MMAs of the item issued
-        umma_commit(&sm.v_empty[st]);
+        if (i + 1 < n) umma_commit_if(leader, &sm.k_empty[stn]);   // every S MMA on K stage stn issued
+        if (i == n - 2) umma_commit_if(leader, &sm.q_empty[qs]);    // last S MMAs of the item issued
+        umma_commit_if(leader, &sm.v_empty[st]);
       }
       kv_cnt += n;
       if (!ok) break;
@@ -518,13 +527,13 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
     bool ok = true;
     if (!s_issued) {
       const int qs = q_cnt % kQSlots;
-      if (!WS_WAIT(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
+      if (!WS_WAIT_WARP(&sm.q_full[qs], (q_cnt / kQSlots) & 1)) break;
       ++q_cnt;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
         if (ok && u.n[t] > 0) ok = pair_s(u, t, q_lo00 + qs * 2 * kStep, kv_cnt);
       if (!ok) break;
-      umma_commit(&sm.q_empty[qs]);
+      umma_commit_if(leader, &sm.q_empty[qs]);
     }
     // the next unit, if paired, gets its S_t issued right after this unit's P_t V
     MmaUnit nx;
@@ -560,27 +569,27 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
       bool progressed = false;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (state[t] == 1 && mbar_test_wait(&sm.p_lo[t], par[t]) && mbar_test_wait(&sm.v_full[st[t]], vpar[t])) {
+        if (state[t] == 1 && warp_test_wait(&sm.p_lo[t], par[t]) && warp_test_wait(&sm.v_full[st[t]], vpar[t])) {
           tc_fence_after();
-          issue_pv<0, 4>(tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, false);
+          issue_pv<0, 4>(leader, tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, false);
           state[t] = 2;
           progressed = true;
         }
-        if (state[t] == 2 && mbar_test_wait(&sm.p_hi[t], par[t])) {
+        if (state[t] == 2 && warp_test_wait(&sm.p_hi[t], par[t])) {
           tc_fence_after();
-          issue_pv<4, 8>(tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, true);
-          umma_commit(&sm.o_full[t]);
-          umma_commit(&sm.v_empty[st[t]]);
+          issue_pv<4, 8>(leader, tO[t], tS[t], v_lo0 + st[t] * kStep, idesc_pv, true);
+          umma_commit_if(leader, &sm.o_full[t]);
+          umma_commit_if(leader, &sm.v_empty[st[t]]);
           state[t] = (ahead && nx.n[t] > 0) ? 3 : 0;
           progressed = true;
         }
         if (state[t] == 3) {
-          if (!q_nx_ready) q_nx_ready = mbar_test_wait(&sm.q_full[qs_nx], q_par_nx);
-          if (q_nx_ready && mbar_test_wait(&sm.k_full[st_nx[t]], kpar_nx[t])) {
+          if (!q_nx_ready) q_nx_ready = warp_test_wait(&sm.q_full[qs_nx], q_par_nx);
+          if (q_nx_ready && warp_test_wait(&sm.k_full[st_nx[t]], kpar_nx[t])) {
             tc_fence_after();
-            issue_qk<DP>(tS[t], q_lo00 + qs_nx * 2 * kStep + t * kStep, k_lo0 + st_nx[t] * kStep, idesc_qk);
-            umma_commit(&sm.s_full[t]);
-            umma_commit(&sm.k_empty[st_nx[t]]);
+            issue_qk<DP>(leader, tS[t], q_lo00 + qs_nx * 2 * kStep + t * kStep, k_lo0 + st_nx[t] * kStep, idesc_qk);
+            umma_commit_if(leader, &sm.s_full[t]);
+            umma_commit_if(leader, &sm.k_empty[st_nx[t]]);
             state[t] = 0;
             progressed = true;
           }
@@ -590,25 +599,30 @@ __device__ void ws_mma(WsSmem<DP>& sm, const AttnParams& p, uint32_t tmem, volat
         idle = 0;
         idle_t0 = 0;
       } else if ((++idle & 255u) == 0) {   // bounded polling, like the other waits
-        if (*abort_flag) { ok = false; break; }
-        const uint64_t now = globaltimer_ns();
+        // lane 0's view, so that the warp decides together
+        if (__shfl_sync(0xffffffffu, *abort_flag != 0u ? 1 : 0, 0) != 0) { ok = false; break; }
+        const uint64_t t = globaltimer_ns();
+        const uint64_t now = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(t >> 32), 0) << 32) |
+                             __shfl_sync(0xffffffffu, (uint32_t)t, 0);
         if (idle_t0 == 0) {
           idle_t0 = now;
         } else if (now - idle_t0 > p.wait_limit_ns) {
-          *abort_flag = 1u;
-          atomicOr(p.status, THD_WAIT_TIMEOUT_BIT);
+          if (leader) {
+            *abort_flag = 1u;
+            atomicOr(p.status, THD_WAIT_TIMEOUT_BIT);
+          }
           ok = false;
         }
       }
     }
     if (!ok) break;
-    if (ahead) umma_commit(&sm.q_empty[qs_nx]);
+    if (ahead) umma_commit_if(leader, &sm.q_empty[qs_nx]);
     kv_cnt = kv_next;
     u = nx;
     s_issued = ahead;
   }
   // every MMA issued so far completes before TMEM is released
-  umma_commit(&sm.drain);
+  umma_commit_if(leader, &sm.drain);
   drain_wait(&sm.drain, 0);
 }
 
@@ -956,7 +970,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   WsSmem<DP>& sm = *reinterpret_cast<WsSmem<DP>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < WsSmem<DP>::kQSlots; ++s) {
       mbar_init(&sm.q_full[s], 1);
@@ -999,8 +1012,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if (warp == 0) {
       ws_producer<DP, kWin, kPack>(sm, p, &tm_q, &tm_k, &tm_v, abort_flag);
     } else if (warp == 1) {
-      if (lane == 0) ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
-      __syncwarp();
+      ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
     } else {
       zero_pad_rows(p, 64, 64, 2);
     }
