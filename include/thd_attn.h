@@ -334,6 +334,21 @@ int thd_attn_merge(const void* out_a, const float* lse_a, const void* out_b, con
  */
 uint64_t thd_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * thd_set_wait_injection — test setting of the failure path: with enable != 0,
+ * every CTA of the attention kernels (forward, windowed forward, no-allocation
+ * forward, backward) called after it makes one wait on a barrier that nothing
+ * completes before the CTA's end.  That wait runs out after the limit of
+ * thd_set_wait_limit_ns whatever the timing of the rest of the pipeline, so the
+ * call sets THD_STATUS_WAIT_TIMEOUT and its CTAs leave through the failure path
+ * (with their copies and MMAs in flight) every time; its output is unspecified.
+ * enable = 0 (the default) turns it off.  Returns the previous setting (0 or 1).
+ *
+ * No counterpart on the pages: it belongs to the library's failure handling and
+ * exists for its tests; nothing faults, traps or hangs.
+ */
+int thd_set_wait_injection(int enable);
+
 /* Human-readable name of a thd_status value (static storage). */
 const char* thd_status_string(int status);
 

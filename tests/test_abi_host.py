@@ -191,3 +191,11 @@ def test_binding_refuses_bad_qkv_before_any_launch(fn):
 
 def test_noalloc_status_rejects_null(lib):
     assert lib.thd_attn_noalloc_status(None, None) == vlp.THD_ERR_ARG
+
+
+def test_wait_injection_setter_round_trip():
+    """The failure-path test setting is off by default and returns its previous value
+    (host state only: no launch)."""
+    assert vlp.thd_set_wait_injection(True) is False
+    assert vlp.thd_set_wait_injection(False) is True
+    assert vlp.thd_set_wait_injection(False) is False

@@ -19,7 +19,7 @@ from thd_testutil import compare_full, compare_sampled, run_gpu, to_device
 pytestmark = pytest.mark.gpu
 vlp = pytest.importorskip("variable_length_packed_gb300")
 
-SHORT_LIMIT_NS = 1   # every wait still pending after its first 16 polls runs out
+SHORT_LIMIT_NS = 1   # a wait still pending after its first poll runs out
 
 
 def status_word(ws):
@@ -31,10 +31,16 @@ def workspace(n=None):
 
 
 class short_waits:
+    """A short wait limit, and the injected wait that runs out whatever the timing (a
+    pipeline fast enough that every wait completes within the hardware's first suspended
+    poll would otherwise let no wait run out)."""
+
     def __enter__(self):
         self.prev = vlp.thd_set_wait_limit_ns(SHORT_LIMIT_NS)
+        assert vlp.thd_set_wait_injection(True) is False
 
     def __exit__(self, *exc):
+        assert vlp.thd_set_wait_injection(False) is True
         assert vlp.thd_set_wait_limit_ns(self.prev) == SHORT_LIMIT_NS
 
 

@@ -15,7 +15,7 @@ import os
 import torch
 
 __all__ = ["thd_attn_fwd", "thd_attn_bwd", "thd_attn_fwd_noalloc", "thd_attn_noalloc_status", "thd_attn_merge", "thd_padding_mask",
-           "thd_padding_mask_cross", "MASK_PADDING", "MASK_PADDING_CAUSAL", "MASK_PADDING_CAUSAL_BOTTOM_RIGHT", "thd_attn_workspace_size", "thd_set_wait_limit_ns", "thd_status_string",
+           "thd_padding_mask_cross", "MASK_PADDING", "MASK_PADDING_CAUSAL", "MASK_PADDING_CAUSAL_BOTTOM_RIGHT", "thd_attn_workspace_size", "thd_set_wait_limit_ns", "thd_set_wait_injection", "thd_status_string",
            "ThdError", "library_path", "load_library", "STATUS_WAIT_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,8 @@ def load_library():
     lib.thd_attn_workspace_size.argtypes = []
     lib.thd_set_wait_limit_ns.restype = ctypes.c_uint64
     lib.thd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.thd_set_wait_injection.restype = ctypes.c_int
+    lib.thd_set_wait_injection.argtypes = [ctypes.c_int]
     lib.thd_status_string.restype = ctypes.c_char_p
     lib.thd_status_string.argtypes = [I]
     _LIB = lib
@@ -91,6 +93,13 @@ def thd_set_wait_limit_ns(ns):
     2 s); returns the previous limit.  A short limit makes waits run out on purpose: the
     call then sets STATUS_WAIT_TIMEOUT in its status word and its output is unspecified."""
     return int(_lib().thd_set_wait_limit_ns(int(ns)))
+
+
+def thd_set_wait_injection(enable):
+    """Test setting of the failure path (see include/thd_attn.h): with enable true, every
+    CTA of a later attention call makes one wait that runs out, so the call reports
+    STATUS_WAIT_TIMEOUT.  Returns the previous setting."""
+    return bool(_lib().thd_set_wait_injection(1 if enable else 0))
 
 
 def thd_status_string(status):

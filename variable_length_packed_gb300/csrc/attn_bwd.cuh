@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
 
   Claimer claimer{0ull, 0};   // used by warp 0
+  bool injected = false;      // thread 0: the test setting's wait was made
   for (;;) {
     if (warp == 0) {
       const unsigned long long w = claim_item(claimer, p);
@@ -254,6 +255,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_2d(sm.v + pn * 16384, &tm_v, &sm.bar_kv, g * p.d + pn * 64, s.kv_start + kv0);
       }
       load_q(g * p.group, s.q_start + qt_first * kTileM);   // the item's first query tile
+      if (p.inject_wait && !injected) {   // test setting: a wait that runs out, loads in flight
+        inject_wait_timeout(p, &sm.bar_drain, abort_flag);
+        injected = true;
+      }
     }
     bool first = true;
     bool stop = false;

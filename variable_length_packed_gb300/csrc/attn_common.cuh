@@ -42,6 +42,7 @@ struct AttnParams {
   uint32_t* status;
   uint64_t wait_limit_ns;  // a pipeline wait gives up (status bit, CTA abort) after this long
   uint32_t wait_check_mask;  // a waiting thread reads the clock when (polls & mask) == 0
+  uint32_t inject_wait;    // test setting: each CTA makes one wait that runs out (inject_wait_timeout)
   int claim;               // work items taken per atomic on the counter (>= 1)
   int win_left, win_right; // sliding window (keys before / after the diagonal), -1 = unbounded
   int B, T, Hq, Hkv, d, group;
@@ -90,6 +91,20 @@ __device__ __forceinline__ int seq_first_key(const SeqInfo& s, int qpos) {
 __device__ __forceinline__ int seq_last_key(const SeqInfo& s, int qpos) {
   const long long l = (long long)qpos + s.shift + s.hi_off;
   return l > s.kv_len - 1 ? s.kv_len - 1 : (l < -1 ? -1 : (int)l);
+}
+
+// Test setting (p.inject_wait, off by default): one bounded wait on phase 0 of `bar`,
+// a barrier that nothing completes before the CTA's own final drain, so the wait runs
+// out after p.wait_limit_ns whatever the timing, sets the status bit and the CTA's
+// abort flag, and the CTA leaves through its failure path with its copies and MMAs in
+// flight.
+__device__ __forceinline__ void inject_wait_timeout(const AttnParams& p, uint64_t* bar, volatile uint32_t* abort) {
+  mbar_wait(bar, 0, abort, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns, p.wait_check_mask);
+}
+// The same by a whole warp, which leaves it together.
+__device__ __forceinline__ bool inject_wait_timeout_warp(const AttnParams& p, uint64_t* bar, volatile uint32_t* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, 0, abort, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
+                                           p.wait_check_mask) ? 1 : 0) != 0;
 }
 
 // Sequence b's rows, clamped to the packed buffer [0, T): garbage metadata

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(128, 1)
   volatile uint32_t* abort_flag = &sm.abort;
 
   Claimer claimer{0ull, 0};   // used by warp 0
+  bool injected = false;      // thread 0: the test setting's wait was made
   for (;;) {
     if (warp == 0) {
       const unsigned long long w = claim_item(claimer, p);
@@ -145,6 +146,10 @@ __global__ void __launch_bounds__(128, 1)
         const int kv0 = j * kBlockN;
         // ---- S = Q K^T ----
         if (tid == 0) {
+          if (p.inject_wait && !injected) {   // test setting: a wait that runs out, loads in flight
+            inject_wait_timeout(p, &sm.bar_drain, abort_flag);
+            injected = true;
+          }
           if (kTMA && mbar_wait(&sm.bar_load, ph_load, abort_flag, p.status, THD_WAIT_TIMEOUT_BIT, p.wait_limit_ns,
                     p.wait_check_mask))
             load_par = -1;

@@ -1015,6 +1015,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       ws_mma<DT, DP, kWin>(sm, p, tmem, abort_flag);
     } else {
       zero_pad_rows(p, 64, 64, 2);
+      // test setting: a wait that runs out while the pipeline runs (the drain barrier
+      // completes only when the MMA warp's last MMAs have, at the CTA's end)
+      if (warp == 3 && p.inject_wait) inject_wait_timeout_warp(p, &sm.drain, abort_flag);
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();

@@ -33,9 +33,15 @@ std::atomic<uint64_t> g_wait_limit_ns{thd::kWaitLimitNs};
 // A waiting thread reads the clock every 256 polls; with a limit under 1 ms
 // (only ever set to make waits run out on purpose) it reads it at every poll,
 // so that a wait the hardware completes within a few polls still runs out.
+// Test setting (thd_set_wait_injection): every CTA of a later call makes one wait on a
+// barrier that nothing completes before the CTA's end, so that wait runs out whatever the
+// timing of the rest of the pipeline.
+std::atomic<uint32_t> g_inject_wait{0u};
+
 void set_wait_fields(thd::AttnParams& p) {
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.wait_check_mask = p.wait_limit_ns < 1000000ull ? 0u : 255u;
+  p.inject_wait = g_inject_wait.load(std::memory_order_relaxed);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -296,6 +302,8 @@ size_t thd_attn_workspace_size(void) { return kWorkspaceBytes; }
 uint64_t thd_set_wait_limit_ns(uint64_t ns) {
   return g_wait_limit_ns.exchange(ns == 0 ? thd::kWaitLimitNs : ns);
 }
+
+int thd_set_wait_injection(int enable) { return (int)g_inject_wait.exchange(enable ? 1u : 0u); }
 
 int thd_padding_mask(const int32_t* cu_seqlens, int batch_size, int max_seqlen, uint8_t* mask, void* stream) {
   if (batch_size < 0 || max_seqlen < 0) return THD_ERR_ARG;
