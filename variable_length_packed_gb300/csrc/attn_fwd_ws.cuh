@@ -344,7 +344,51 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     ++it_cnt;
     if (!u.valid || !ok) break;
-    if (lane == 0 && u.n_all > 0) {
+    if (kPack) {
+      // the packing instantiation (many short units): the whole warp walks the loads, its
+      // waits and counters warp-uniform, and lane 0 arms the barriers and issues the
+      // predicated copies
+      if (u.n_all > 0) {
+        const bool issue = lane == 0;
+        const int qs = q_cnt % kQSlots;
+        if (q_cnt >= (uint32_t)kQSlots) ok = WS_WAIT_WARP(&sm.q_empty[qs], ((q_cnt / kQSlots) - 1) & 1);
+        if (ok) {
+          const int ntiles = (u.t[0].n > 0 ? 1 : 0) + (u.t[1].n > 0 ? 1 : 0);
+          if (issue) mbar_arrive_expect_tx(&sm.q_full[qs], ntiles * kTileBytes);
+          for (int t = 0; t < 2; ++t) {
+            if (u.t[t].n == 0) continue;   // no S MMA reads this tile
+#pragma unroll
+            for (int pn = 0; pn < kPanels; ++pn)
+              tma_load_2d_if(issue, sm.q[qs][t] + pn * 16384, tm_q, &sm.q_full[qs], u.t[t].h * p.d + pn * 64,
+                             u.t[t].seq.q_start + u.t[t].q0);
+          }
+          ++q_cnt;
+        }
+        for (int li = 0; ok && li < u.n_all; ++li) {
+          const int tsel = (u.paired && !(li == 0 && u.t[0].n > 0)) ? 1 : 0;
+          const int row = (tsel ? u.t[1].seq.kv_start : u.t[0].seq.kv_start) + (u.paired ? 0 : (u.jb + li) * kBlockN);
+          const int kvh = (tsel ? u.t[1].h : u.t[0].h) / p.group;
+          const int st = kv_cnt % kWsStages;
+          const uint32_t reuse = ((kv_cnt / kWsStages) - 1) & 1;
+          if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT_WARP(&sm.k_empty[st], reuse);
+          if (!ok) break;
+          if (issue) mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+#pragma unroll
+          for (int pn = 0; pn < kPanels; ++pn)
+            tma_load_2d_if(issue, sm.k[st] + pn * 16384, tm_k, &sm.k_full[st], kvh * p.d + pn * 64, row);
+          if (kv_cnt >= (uint32_t)kWsStages) ok = WS_WAIT_WARP(&sm.v_empty[st], reuse);
+          if (!ok) {   // the K copy just issued lands before the CTA can exit
+            drain_wait(&sm.k_full[st], (kv_cnt / kWsStages) & 1);
+            break;
+          }
+          if (issue) mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+#pragma unroll
+          for (int pn = 0; pn < kPanels; ++pn)
+            tma_load_2d_if(issue, sm.v[st] + pn * 16384, tm_v, &sm.v_full[st], kvh * p.d + pn * 64, row);
+          ++kv_cnt;
+        }
+      }
+    } else if (lane == 0 && u.n_all > 0) {
       const int qs = q_cnt % kQSlots;
       if (q_cnt >= (uint32_t)kQSlots) ok = WS_WAIT(&sm.q_empty[qs], ((q_cnt / kQSlots) - 1) & 1);
       if (ok) {
