@@ -84,3 +84,29 @@ def test_noalloc_python_wrapper(lib, name, with_lse):
             ldiff = torch.where(both_inf, torch.zeros_like(lse), (lse - ref_lse).abs()).max().item()
             assert ldiff <= LSE_ATOL, (call, ldiff)
         assert not torch.isnan(out).any()
+
+
+def test_noalloc_reports_a_wait_that_ran_out(lib):
+    """A wait that runs out inside the no-allocation call (the failure path's test setting:
+    a 1 ns limit and the injected wait) is reported through thd_attn_noalloc_status, and the
+    next normal call clears the word and gives the bits of a call made before it."""
+    w = workloads.make("long_context_small")
+    dev = to_device(w)
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((w.num_heads_q, w.total_tokens), dtype=torch.float32, device="cuda")
+    args = (dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"], dev["padded"], dev["causal"],
+            w.batch_size, w.max_seqlen, w.softmax_scale, out, lse)
+    before = [t.clone() for t in vlp.thd_attn_fwd_noalloc(*args)]
+    assert vlp.thd_attn_noalloc_status() == 0
+    prev = vlp.thd_set_wait_limit_ns(1)
+    assert vlp.thd_set_wait_injection(True) is False
+    try:
+        vlp.thd_attn_fwd_noalloc(*args)
+        status = vlp.thd_attn_noalloc_status()
+    finally:
+        assert vlp.thd_set_wait_injection(False) is True
+        assert vlp.thd_set_wait_limit_ns(prev) == 1
+    assert status & vlp.STATUS_WAIT_TIMEOUT, status
+    after = vlp.thd_attn_fwd_noalloc(*args)
+    assert vlp.thd_attn_noalloc_status() == 0
+    assert torch.equal(after[0], before[0]) and torch.equal(after[1], before[1])
