@@ -616,24 +616,16 @@ __device__ __forceinline__ void sched_init(SchedSmem& s) {
 // Pad rows: every output row outside all [start_b, start_b + len_b) ranges is
 // written as exact zeros (and -inf LSE).  Gap g (0 <= g <= B) is the range
 // between the end of sequence g-1 (0 for g == 0) and the start of sequence g
-// (T for g == B).  Gaps are spread over CTAs; `nthreads` threads starting at
-// thread `t0` of the CTA take part.
+// (T for g == B).  Gaps before a sequence are spread over CTAs, one CTA each; the
+// trailing gap, which is most of the buffer when the buffer holds more rows than
+// the batch (T sized for a larger batch), is split over all CTAs in equal shares.
+// `nthreads` threads starting at thread `t0` of the CTA take part.
 // ----------------------------------------------------------------------------
 __device__ void zero_pad_rows(const AttnParams& p, int t0, int nthreads, int elem_bytes) {
   const int tid = (int)threadIdx.x - t0;
   const long long row_bytes = (long long)p.Hq * p.d * elem_bytes;
-  for (int g = blockIdx.x; g <= p.B; g += gridDim.x) {
-    long long a = 0, e = p.T;
-    if (g > 0) {
-      SeqInfo s = load_seq(p, g - 1);
-      a = (long long)s.q_start + s.q_len;
-    }
-    if (g < p.B) {
-      const long long cq = p.cu_q[g];
-      long long st = p.pad_q ? (long long)p.pad_q[g] : cq;
-      e = st < 0 ? 0 : (st > p.T ? p.T : st);
-    }
-    if (e <= a) continue;
+  auto zero_rows = [&](long long a, long long e) {   // rows [a, e)
+    if (e <= a) return;
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(p.out) + a * row_bytes);
     const long long n16 = (e - a) * row_bytes / 16;
     for (long long i = tid; i < n16; i += nthreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -644,7 +636,25 @@ __device__ void zero_pad_rows(const AttnParams& p, int t0, int nthreads, int ele
         p.lse[h * p.T + a + r] = -INFINITY;
       }
     }
+  };
+  for (int g = blockIdx.x; g < p.B; g += gridDim.x) {
+    long long a = 0;
+    if (g > 0) {
+      SeqInfo s = load_seq(p, g - 1);
+      a = (long long)s.q_start + s.q_len;
+    }
+    const long long cq = p.cu_q[g];
+    const long long st = p.pad_q ? (long long)p.pad_q[g] : cq;
+    zero_rows(a, st < 0 ? 0 : (st > p.T ? p.T : st));
   }
+  long long a = 0;   // the trailing gap [end of the last sequence, T), this CTA's share
+  if (p.B > 0) {
+    SeqInfo s = load_seq(p, p.B - 1);
+    a = (long long)s.q_start + s.q_len;
+  }
+  const long long rows = (long long)p.T - a;
+  if (rows > 0)
+    zero_rows(a + rows * blockIdx.x / gridDim.x, a + rows * (blockIdx.x + 1) / gridDim.x);
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` of a 128-row tile stored as
