@@ -328,6 +328,23 @@ def test_gap_contents_do_not_leak():
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
 
 
+@pytest.mark.parametrize("hint,d", [(140, 64), (4096, 128)])   # the packing and the plain instantiation
+def test_large_trailing_region_is_zeroed(hint, d):
+    """A buffer with many more rows than the batch holds (T sized for a larger batch): the
+    rows after the last sequence, which every CTA zeroes a share of, are exact zeros with
+    -inf LSE over outputs that held NaN, and the sequences' rows match the oracle."""
+    w = workloads.from_lengths("trail", [100, 300, 37], [1, 0, 1], gaps_before=[5, 0, 9], trailing=40000,
+                               heads_q=4, head_dim=d, dtype=torch.bfloat16, seed=15)
+    dev = to_device(w)
+    out = torch.full_like(dev["q"], float("nan"))
+    lse = torch.full((w.num_heads_q, w.total_tokens), float("nan"), dtype=torch.float32, device="cuda")
+    vlp.thd_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], dev["cu"], dev["padded"], dev["padded"],
+                     dev["causal"], w.batch_size, hint, w.softmax_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_pad_rows(w, out, lse)
+    compare_full(w, out, lse)
+
+
 def test_garbage_past_batch_is_ignored_and_deterministic():
     w = workloads.from_lengths("tail", [50, 260, 9], [0, 1, 1], heads_q=2, head_dim=64, dtype=torch.float16,
                                seed=13, capacity=16, rng=np.random.default_rng(5))

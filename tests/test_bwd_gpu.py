@@ -110,6 +110,16 @@ def test_mixed_lengths_and_groups(d, dtype, group):
     check(w, got, ref, f"mix d{d} g{group}", layout_zeros(w), bounds)
 
 
+def test_large_trailing_region():
+    """T far above the batch's rows: dK / dV of the rows after the last sequence (zeroed by
+    every block of the first launch in equal shares) are exact zeros, dQ there too, and
+    the sequences' gradients are within the per-element bounds."""
+    w = workloads.from_lengths("trail", [100, 300, 37], [1, 0, 1], gaps_before=[5, 0, 9], trailing=30000,
+                               heads_q=4, heads_kv=2, head_dim=128, dtype=torch.bfloat16, seed=16)
+    got, ref, bounds = run_bwd(w, seed=17)
+    check(w, got, ref, "trail", layout_zeros(w), bounds)
+
+
 def test_mask_types_separate_q_kv():
     import test_merge_gpu as tm
     w, cu_q, cu_k, qs, ks, codes = tm.rect_batch(128, torch.bfloat16, seed=5)

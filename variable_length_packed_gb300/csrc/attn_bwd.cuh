@@ -43,23 +43,33 @@ struct BwdParams {
 // ---------------------------------------------------------------------------
 // pre
 // ---------------------------------------------------------------------------
-// Rows of no key/value sequence: gap g lies between key/value spans g-1 and g.
+// Rows of no key/value sequence: gap g lies between key/value spans g-1 and g (the
+// gaps before a span one block each; the trailing region after the last span, which
+// is most of the buffer when it holds more rows than the batch, in equal shares over
+// all blocks).
 __device__ void zero_kv_gap_rows(const AttnParams& p, void* dst, long long row_bytes) {
-  for (int g = blockIdx.x; g <= p.B; g += gridDim.x) {
-    long long a = 0, e = p.T;
+  auto zero_rows = [&](long long a, long long e) {   // rows [a, e)
+    if (e <= a) return;
+    uint4* d4 = reinterpret_cast<uint4*>(static_cast<char*>(dst) + a * row_bytes);
+    const long long n16 = (e - a) * row_bytes / 16;
+    for (long long i = threadIdx.x; i < n16; i += blockDim.x) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+  };
+  for (int g = blockIdx.x; g < p.B; g += gridDim.x) {
+    long long a = 0;
     if (g > 0) {
       SeqInfo s = load_seq(p, g - 1);
       a = (long long)s.kv_start + s.kv_len;
     }
-    if (g < p.B) {
-      const long long st = p.pad_kv ? (long long)p.pad_kv[g] : (long long)p.cu_kv[g];
-      e = st < 0 ? 0 : (st > p.T ? p.T : st);
-    }
-    if (e <= a) continue;
-    uint4* d4 = reinterpret_cast<uint4*>(static_cast<char*>(dst) + a * row_bytes);
-    const long long n16 = (e - a) * row_bytes / 16;
-    for (long long i = threadIdx.x; i < n16; i += blockDim.x) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+    const long long st = p.pad_kv ? (long long)p.pad_kv[g] : (long long)p.cu_kv[g];
+    zero_rows(a, st < 0 ? 0 : (st > p.T ? p.T : st));
   }
+  long long a = 0;
+  if (p.B > 0) {
+    SeqInfo s = load_seq(p, p.B - 1);
+    a = (long long)s.kv_start + s.kv_len;
+  }
+  const long long rows = (long long)p.T - a;
+  if (rows > 0) zero_rows(a + rows * blockIdx.x / gridDim.x, a + rows * (blockIdx.x + 1) / gridDim.x);
 }
 
 template <typename DT>
