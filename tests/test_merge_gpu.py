@@ -31,6 +31,39 @@ def rect_batch(d, dtype, seed):
     return w, cu_q, cu_k, np.array(qs, np.int32), np.array(ks, np.int32), np.array(codes, np.uint8)
 
 
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float16)])
+def test_packed_short_sequences_with_separate_q_kv(d, dtype):
+    """The packing instantiation (a max_seqlen hint of 128) on 300 short sequences whose
+    query and key/value spans differ in length and position, with every mask type and
+    sequences without keys; rows of no sequence and rows that see no key: zero out, -inf LSE."""
+    rng = np.random.default_rng(d + 1)
+    B = 300
+    lq = rng.integers(1, 101, B)
+    lkv = np.where(rng.random(B) < 0.05, 0, rng.integers(1, 121, B))
+    codes = rng.integers(0, 3, B).astype(np.uint8)
+    qs = np.cumsum(np.r_[0, lq[:-1] + rng.integers(0, 6, B - 1)])
+    ks = qs[-1] + lq[-1] + 7 + np.cumsum(np.r_[0, lkv[:-1] + rng.integers(0, 6, B - 1)])
+    T = int(ks[-1] + lkv[-1] + 3)
+    w = workloads.from_lengths("rect_short", [T], [0], heads_q=4, heads_kv=2, head_dim=d, dtype=dtype, seed=d + 2)
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int32)
+    qs, ks = qs.astype(np.int32), ks.astype(np.int32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    out, lse = vlp.thd_attn_fwd(q, k, v, dev(cu_q), dev(cu_k), dev(qs), dev(ks), dev(codes), B, 128,
+                                w.softmax_scale)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.thd_attention_fwd_general(w.q, w.k, w.v, cu_q, cu_k, qs, ks, codes, B, w.softmax_scale)
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    seen = np.isfinite(ref_lse)
+    assert_out_close(o, ref, dtype, "packed cross")
+    assert np.abs(l[seen] - ref_lse[seen]).max() <= LSE_ATOL
+    assert np.all(np.isneginf(l[~seen]))
+    rows_none = ~seen.any(axis=0)
+    assert np.all(o[rows_none] == 0)
+
+
 @pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float16), (40, torch.bfloat16)])
 def test_mask_types_with_separate_q_kv(d, dtype):
     w, cu_q, cu_k, qs, ks, codes = rect_batch(d, dtype, seed=d)
