@@ -302,6 +302,12 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   uint32_t it_cnt = 0, q_cnt = 0, kv_cnt = 0;
   bool ok = true;
   Claimer claimer{0ull, 0};
+  // The packing instantiation claims half-size batches one batch ahead (lane 0 holds the
+  // current batch and the next one, whose atomic is in flight while the current one runs),
+  // so a CTA still holds at most p.claim unstarted units; claimed indices still increase.
+  unsigned long long ahead_cur = 0, ahead_nxt = 0, ahead_base = 0;
+  int ahead_left = 0;
+  bool ahead_init = false;
   // packed tiles: the (chunk, group) whose row table each slot's tile holds,
   // as chunk_base * 1024 + group + 1 (group -1: a tile without rows, whose table
   // marks every row absent), -1 while the slot has none (slot 0 tiles 0, 1, then
@@ -309,7 +315,29 @@ __device__ void ws_producer(WsSmem<DP>& sm, const AttnParams& p, const CUtensorM
   // slot and group
   long long rows_of[4] = {-1, -1, -1, -1};
   for (;;) {
-    const unsigned long long w = claim_item(claimer, p);
+    unsigned long long w;
+    if (kPack) {   // half-size batches, the next one's atomic in flight while this one runs
+      const int c = p.claim > 1 ? p.claim / 2 : 1;
+      if (ahead_left == 0) {
+        unsigned long long b = 0;
+        if (lane == 0) {
+          if (!ahead_init) {
+            ahead_cur = atomicAdd(p.work_counter, (unsigned long long)c);
+            ahead_init = true;
+          } else {
+            ahead_cur = ahead_nxt;
+          }
+          ahead_nxt = atomicAdd(p.work_counter, (unsigned long long)c);
+          b = ahead_cur;
+        }
+        ahead_base = __shfl_sync(0xffffffffu, b, 0);
+        ahead_left = c;
+      }
+      w = ahead_base + (unsigned long long)(c - ahead_left);
+      --ahead_left;
+    } else {
+      w = claim_item(claimer, p);
+    }
     WsUnit u = ws_decode<kWin, kPack>(sm.sched, p, w);
     const int slot = it_cnt & 1;
     if (kPack && u.valid && u.packed) {
