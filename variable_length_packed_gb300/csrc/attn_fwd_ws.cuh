@@ -10,10 +10,11 @@
 //               publishes them to the other warps, loads Q (both tiles) and the
 //               K/V tiles of the item into a ring (2 stages at head_dim 128, 4
 //               at 64).
-//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM (SS UMMA),
-//               then O_i += P_i V_j with P_i read from TMEM (TS UMMA); the two
-//               tiles alternate so one tile's softmax overlaps the other
-//               tile's MMAs.
+//   warp 1      MMA issuer: S_i = Q_i K_j^T into TMEM (SS UMMA), then
+//               O_i += P_i V_j with P_i read from TMEM (TS UMMA); the two tiles
+//               alternate so one tile's softmax overlaps the other tile's MMAs.
+//               The whole warp runs the loop converged (descriptors and waits
+//               warp-uniform) and one elected lane issues the MMAs and commits.
 //   warps 2-3   write the pad rows' zeros, then wait at the end.
 //   warps 4-7   softmax of Q tile 0; warps 8-11 softmax of Q tile 1.  One thread
 //               per query row (= TMEM lane): masking, online max / sum, P
